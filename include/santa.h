@@ -1,0 +1,133 @@
+/*
+ * santa.h -- C ABI of libsanta.so: GB300-native (sm_103a) SANTA decode-step attention.
+ *
+ * The operation ("Stochastic Sparse Attention for Memory-Bound Inference", abstract):
+ * one autoregressive decode step of attention over a long KV cache.  For every batch
+ * row b and query head h (KV head g = h / (H_q / H_kv), grouped-query attention), the
+ * score stage reads all n_b cached keys and forms p = softmax(scale * q K^T).  The value
+ * stage does not compute the dense p.V product.  It draws S << n_b key indices from p by
+ * stratified or systematic sampling and returns (1/S) * sum of the S sampled V rows:
+ * a gather-and-add with no multiply per key, and an unbiased estimator of p.V.
+ * SANTA_DENSE computes the exact p.V with the same score machinery, as the
+ * like-for-like baseline (the pages compare against split-K decode kernels).
+ *
+ * Conventions for every entry point:
+ *  - Device pointers are plain CUDA device addresses; ownership stays with the caller.
+ *    The library allocates nothing and keeps no state between calls beyond what it
+ *    writes into the caller's workspace.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is enqueued
+ *    asynchronously on it; the library never synchronises the host, except in
+ *    santa_device_status.
+ *  - Return value: SANTA_OK (0) or a negative status; see santa_status_string.  Argument
+ *    errors are detected on the host before anything is enqueued.
+ */
+#ifndef SANTA_H_
+#define SANTA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define SANTA_OK 0
+#define SANTA_ERR_INVALID_ARG (-1)  /* null pointer, bad shape, bad S or mode */
+#define SANTA_ERR_MISALIGNED (-2)   /* a pointer is not 16-byte aligned */
+#define SANTA_ERR_WORKSPACE (-3)    /* workspace missing or smaller than required */
+#define SANTA_ERR_UNSUPPORTED (-4)  /* valid but outside the compiled limits (d, G, S, B) */
+#define SANTA_ERR_CUDA (-5)         /* a CUDA launch or runtime call failed */
+#define SANTA_ERR_DEVICE (-6)       /* the device reported an error (santa_device_status) */
+
+/* Value-stage modes ("stratified and systematic sampling", abstract; iid is plain
+ * multinomial sampling, the estimator before variance reduction). */
+#define SANTA_DENSE 0
+#define SANTA_STRATIFIED 1
+#define SANTA_SYSTEMATIC 2
+#define SANTA_IID 3
+
+/* Device error bits (santa_device_status). */
+#define SANTA_DEV_BAD_SEQLEN 1      /* some seq_lens[b] outside [0, n_max]; treated as 0 */
+#define SANTA_DEV_TIMEOUT 2         /* a bounded wait on a shared-memory barrier gave up */
+
+/* Problem shape.  scale = 0 selects 1/sqrt(d) rounded to fp32. */
+typedef struct {
+    int32_t B;      /* batch rows, 1..1024 */
+    int32_t H_q;    /* query heads */
+    int32_t H_kv;   /* KV heads; G = H_q / H_kv must be 1, 2, 4 or 8 */
+    int32_t d;      /* head dimension: 64 or 128 */
+    int32_t n_max;  /* KV-cache capacity per (b, h_kv), 1..524288 */
+    float scale;    /* score scale */
+} santa_shape;
+
+/*
+ * santa_workspace_size -- bytes of device workspace santa_decode needs for this shape,
+ * S and mode.  Pure host computation.
+ * Returns SANTA_OK, SANTA_ERR_INVALID_ARG or SANTA_ERR_UNSUPPORTED.
+ */
+int santa_workspace_size(const santa_shape *shape, int32_t S, int32_t mode, size_t *bytes);
+
+/*
+ * santa_workspace_init -- zero the workspace's control block (counters and the device
+ * error word) on `stream`.  Call once after allocating a workspace; every completed
+ * santa_decode leaves the counters at zero again.  Call it again after an error.
+ */
+int santa_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * santa_decode -- one decode step of SANTA attention (or dense attention).
+ *
+ *  q         device bf16 [B, H_q, d], contiguous
+ *  k_cache   device bf16 [B, H_kv, n_max, d], contiguous; keys j >= seq_lens[b] unused
+ *  v_cache   device bf16 [B, H_kv, n_max, d], contiguous
+ *  seq_lens  device int32 [B], each in [0, n_max]; out-of-range values are treated as 0
+ *            and set SANTA_DEV_BAD_SEQLEN in the device error word
+ *  S         samples per (b, h): 1..4096 (ignored for SANTA_DENSE)
+ *  mode      SANTA_DENSE, SANTA_STRATIFIED, SANTA_SYSTEMATIC or SANTA_IID
+ *  seed      Philox4x64-10 key word 0 (ignored for SANTA_DENSE)
+ *  out       device fp32 [B, H_q, d]; n_b = 0 gives zeros
+ *  idx_out   device int32 [B, H_q, S] or NULL: the sampled key indices of each (b, h),
+ *            ascending, with repeats; n_b = 0 gives -1 (ignored for SANTA_DENSE)
+ *  workspace device buffer of at least santa_workspace_size bytes, 256-byte aligned,
+ *            initialised once by santa_workspace_init; one call at a time per workspace
+ *
+ * The sample points of (b, h) are t_s = (u + s) * r_S (systematic, one uniform u) or
+ * t_s = (s + u_s) * r_S (stratified, one uniform per stratum), s = 0..S-1, with r_S the
+ * fp64 value nearest 1/S; iid draws S uniforms and sorts them.  Uniforms are the top 32
+ * bits of Philox4x64-10 words (Salmon et al., SC'11) times 2^-32, keyed (seed, 0) with
+ * counter (block, b, h, 1 | 2 | 3 for stratified | systematic | iid).  Index
+ * i_s = min{ j : C_j > t_s } on the CDF of p, i.e. point s selects key j when
+ * t_s lies in [C_{j-1}, C_j).
+ */
+int santa_decode(const santa_shape *shape, const void *q, const void *k_cache,
+                 const void *v_cache, const int32_t *seq_lens, int32_t S, int32_t mode,
+                 uint64_t seed, float *out, int32_t *idx_out, void *workspace,
+                 size_t workspace_bytes, void *stream);
+
+/*
+ * santa_sample_points -- the fp64 sample points t [B, H_q, S] (device) that santa_decode
+ * uses for (mode, seed), computed by the same device code.  For checking the sampler's
+ * random stream against an independent implementation.  mode must be a sampling mode.
+ */
+int santa_sample_points(int32_t B, int32_t H_q, int32_t S, int32_t mode, uint64_t seed,
+                        double *t_out, void *stream);
+
+/*
+ * santa_device_status -- synchronise `stream`, read the device error word of the
+ * workspace into *code (0 = no error; SANTA_DEV_* bits otherwise) and clear it.
+ * Returns SANTA_OK, or SANTA_ERR_DEVICE when *code != 0.
+ */
+int santa_device_status(void *workspace, int32_t *code, void *stream);
+
+/* santa_status_string -- static description of a status code. */
+const char *santa_status_string(int status);
+
+/* santa_version -- library version as 10000*major + 100*minor + patch. */
+int santa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SANTA_H_ */

@@ -25,9 +25,12 @@
  *
  * Points (abstract: "stratified and systematic sampling"; the pages give no formula,
  * so the plainest unbiased readings are used):
- *   systematic:  one uniform u per (b,h);  t_s = (u + s) / S
- *   stratified:  one uniform u_s per stratum;  t_s = (s + u_s) / S
+ *   systematic:  one uniform u per (b,h);  t_s = (u + s) * r_S
+ *   stratified:  one uniform u_s per stratum;  t_s = (s + u_s) * r_S
  *   iid:         S independent uniforms, sorted ascending
+ * with r_S = 1/S rounded once to fp64: the pages leave the arithmetic open, and one
+ * correctly rounded multiply is reproducible bit for bit by any IEEE implementation
+ * (u + s is exact, since u has 32 fraction bits and s < 2^21).
  * Uniforms: the top 32 bits of a Philox4x64-10 word times 2^-32 (an exact fp64 in
  * [0, 1 - 2^-32]).  Philox4x64-10 is the counter-based generator of Salmon, Moraes,
  * Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC'11), written here
@@ -111,11 +114,13 @@ int oracle_points(int mode, int32_t S, uint64_t seed, int32_t b, int32_t h, doub
         uint64_t r[4];
         oracle_philox4x64_10(ctr, key, r);
         const double u = word_to_uniform(r[0]);
-        for (int32_t s = 0; s < S; ++s) t[s] = (u + (double)s) / (double)S;
+        const double rS = 1.0 / (double)S;
+        for (int32_t s = 0; s < S; ++s) t[s] = (u + (double)s) * rS;
         return 0;
     }
     if (mode == ORC_STRATIFIED || mode == ORC_IID) {
         const uint64_t dom = (mode == ORC_STRATIFIED) ? 1 : 3;
+        const double rS = 1.0 / (double)S;
         uint64_t r[4];
         for (int32_t s = 0; s < S; ++s) {
             if (s % 4 == 0) {
@@ -123,7 +128,7 @@ int oracle_points(int mode, int32_t S, uint64_t seed, int32_t b, int32_t h, doub
                 oracle_philox4x64_10(ctr, key, r);
             }
             const double u = word_to_uniform(r[s % 4]);
-            t[s] = (mode == ORC_STRATIFIED) ? ((double)s + u) / (double)S : u;
+            t[s] = (mode == ORC_STRATIFIED) ? ((double)s + u) * rS : u;
         }
         if (mode == ORC_IID) qsort(t, (size_t)S, sizeof(double), cmp_double);
         return 0;
