@@ -1,0 +1,348 @@
+// santa_api.cu -- the C ABI of libsanta.so (declared in include/santa.h): argument
+// checks, workspace carve-up, split planning and kernel dispatch.  No allocation, no
+// host synchronisation (except santa_device_status), no CPU fallback.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/santa.h"
+#include "santa_dense.cuh"
+#include "santa_kernels.h"
+
+namespace santa {
+
+int sample_smem_bytes(int D, int G, int B, int S, int ns_used, int mode)
+{
+    return sample_smem(D, G, B, S, ns_used, mode).total;
+}
+
+int dense_smem_bytes(int D, int G, int B)
+{
+    return dense_smem(D, G, B, 2).total;
+}
+
+// ---------------------------------------------------------------- points kernels
+
+__global__ void santa_points_kernel(int B, int H_q, int S, int mode, uint64_t seed, double rS, double *t)
+{
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t total = (size_t)B * H_q * S;
+    if (i >= total) return;
+    const int s = (int)(i % S);
+    const int h = (int)((i / S) % H_q);
+    const int b = (int)(i / ((size_t)S * H_q));
+    t[i] = sample_point(mode, seed, b, h, s, rS);
+}
+
+// iid: one CTA per (b, h) sorts its S draws (bitonic, in shared memory).
+__global__ void santa_points_iid_kernel(int B, int H_q, int S, uint64_t seed, double *t)
+{
+    __shared__ unsigned keys[SMAX];
+    const int bh = blockIdx.x;
+    const int b = bh / H_q, h = bh % H_q;
+    int Sp = 1;
+    while (Sp < S) Sp <<= 1;
+    for (int s = threadIdx.x; s < Sp; s += blockDim.x) {
+        unsigned u = 0xffffffffu;
+        if (s < S) {
+            uint64_t rnd[4];
+            philox_block(seed, (uint64_t)(s / 4), b, h, 3, rnd);
+            u = (unsigned)(rnd[s % 4] >> 32);
+        }
+        keys[s] = u;
+    }
+    __syncthreads();
+    for (int k = 2; k <= Sp; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int s = threadIdx.x; s < Sp; s += blockDim.x) {
+                const int q = s ^ j;
+                if (q > s) {
+                    const bool asc = (s & k) == 0;
+                    const unsigned x = keys[s], y = keys[q];
+                    if ((x > y) == asc) {
+                        keys[s] = y;
+                        keys[q] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    for (int s = threadIdx.x; s < S; s += blockDim.x)
+        t[(size_t)bh * S + s] = __dmul_rn(__uint2double_rn(keys[s]), 0x1p-32);
+}
+
+const void *points_kernel() { return (const void *)santa_points_kernel; }
+const void *points_iid_kernel() { return (const void *)santa_points_iid_kernel; }
+
+// ---------------------------------------------------------------- per-device caches
+
+namespace {
+
+constexpr int MAX_DEV = 64;
+std::mutex g_mu;
+int g_sms[MAX_DEV];
+int g_optin[MAX_DEV];
+
+struct FnCache {
+    const void *fn;
+    int dev, smem_set, occ_smem, occ;
+};
+FnCache g_fn[256];
+int g_nfn = 0;
+
+int device_info(int *dev, int *sms, int *optin)
+{
+    if (cudaGetDevice(dev) != cudaSuccess) return SANTA_ERR_CUDA;
+    if (*dev < 0 || *dev >= MAX_DEV) return SANTA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sms[*dev] == 0) {
+        int a = 0, b = 0;
+        if (cudaDeviceGetAttribute(&a, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess) return SANTA_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&b, cudaDevAttrMaxSharedMemoryPerBlockOptin, *dev) != cudaSuccess)
+            return SANTA_ERR_CUDA;
+        g_sms[*dev] = a;
+        g_optin[*dev] = b;
+    }
+    *sms = g_sms[*dev];
+    *optin = g_optin[*dev];
+    return SANTA_OK;
+}
+
+// Raise the kernel's dynamic shared-memory limit if needed; return CTAs per SM.
+int prepare_fn(const void *fn, int dev, int smem, int *occ)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    FnCache *c = nullptr;
+    for (int i = 0; i < g_nfn; ++i)
+        if (g_fn[i].fn == fn && g_fn[i].dev == dev) c = &g_fn[i];
+    if (!c) {
+        if (g_nfn == 256) return SANTA_ERR_UNSUPPORTED;
+        c = &g_fn[g_nfn++];
+        c->fn = fn;
+        c->dev = dev;
+        c->smem_set = 0;
+        c->occ_smem = -1;
+        c->occ = 0;
+    }
+    if (smem > 48 * 1024 && smem > c->smem_set) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return SANTA_ERR_CUDA;
+        c->smem_set = smem;
+    }
+    if (c->occ_smem != smem) {
+        int o = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, fn, NT, smem) != cudaSuccess) return SANTA_ERR_CUDA;
+        c->occ = o;
+        c->occ_smem = smem;
+    }
+    *occ = c->occ;
+    return *occ > 0 ? SANTA_OK : SANTA_ERR_UNSUPPORTED;
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_shape(const santa_shape *sh)
+{
+    if (!sh) return SANTA_ERR_INVALID_ARG;
+    if (sh->B < 1 || sh->H_q < 1 || sh->H_kv < 1 || sh->n_max < 1 || sh->d < 1) return SANTA_ERR_INVALID_ARG;
+    if (sh->H_q % sh->H_kv != 0) return SANTA_ERR_INVALID_ARG;
+    if (!std::isfinite(sh->scale)) return SANTA_ERR_INVALID_ARG;
+    const int G = sh->H_q / sh->H_kv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return SANTA_ERR_UNSUPPORTED;
+    if (sh->d != 64 && sh->d != 128) return SANTA_ERR_UNSUPPORTED;
+    if (sh->B > BMAX || sh->H_q > 1024) return SANTA_ERR_UNSUPPORTED;
+    if ((long long)sh->n_max > (long long)NS_LIMIT * LMAX) return SANTA_ERR_UNSUPPORTED;
+    return SANTA_OK;
+}
+
+int check_mode_S(int32_t mode, int32_t S)
+{
+    if (mode < SANTA_DENSE || mode > SANTA_IID) return SANTA_ERR_INVALID_ARG;
+    if (mode != SANTA_DENSE && (S < 1 || S > SMAX)) return SANTA_ERR_INVALID_ARG;
+    return SANTA_OK;
+}
+
+// Split length: the longest of 1024/512/256 keys that still gives every SM at least
+// four work items, and at most NS_LIMIT splits per sequence.
+int choose_L(const santa_shape *sh, int sms)
+{
+    const int cand[3] = {1024, 512, 256};
+    const long long groups = (long long)sh->B * sh->H_kv;
+    int L = LMIN;
+    for (int i = 0; i < 3; ++i) {
+        const long long ns = (sh->n_max + cand[i] - 1) / cand[i];
+        if (groups * ns >= 4LL * sms) {
+            L = cand[i];
+            break;
+        }
+    }
+    while ((sh->n_max + L - 1) / L > NS_LIMIT) L *= 2;
+    return L;
+}
+
+}  // namespace
+}  // namespace santa
+
+using namespace santa;
+
+extern "C" {
+
+int santa_version(void) { return 10000; }
+
+const char *santa_status_string(int status)
+{
+    switch (status) {
+    case SANTA_OK: return "ok";
+    case SANTA_ERR_INVALID_ARG: return "invalid argument";
+    case SANTA_ERR_MISALIGNED: return "pointer not aligned (16 bytes for tensors, 256 for the workspace)";
+    case SANTA_ERR_WORKSPACE: return "workspace missing or too small";
+    case SANTA_ERR_UNSUPPORTED: return "outside the supported limits (d in {64,128}, G in {1,2,4,8}, B <= 1024, "
+                                      "n_max <= 524288, S <= 4096, shared memory)";
+    case SANTA_ERR_CUDA: return "CUDA runtime error";
+    case SANTA_ERR_DEVICE: return "device reported an error (bad seq_lens or a barrier timeout)";
+    default: return "unknown status";
+    }
+}
+
+int santa_workspace_size(const santa_shape *shape, int32_t S, int32_t mode, size_t *bytes)
+{
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if ((rc = check_mode_S(mode, S))) return rc;
+    if (!bytes) return SANTA_ERR_INVALID_ARG;
+    *bytes = ws_layout(shape->B, shape->H_q, shape->H_kv, shape->d, shape->n_max, mode == SANTA_DENSE).total;
+    return SANTA_OK;
+}
+
+int santa_workspace_init(void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!workspace) return SANTA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return SANTA_ERR_MISALIGNED;
+    const size_t n = workspace_bytes < 256 ? workspace_bytes : 256;
+    if (n < sizeof(int) * 4) return SANTA_ERR_WORKSPACE;
+    // The control block is CTRL_GROUPS words plus one counter per group; the caller's
+    // workspace may be shared across shapes, so clear every counter word it can hold
+    // up to the first data region (a conservative 64 KiB bound).
+    size_t ctrl = workspace_bytes < (size_t)65536 ? workspace_bytes : (size_t)65536;
+    ctrl = ctrl / 4 * 4;
+    if (cudaMemsetAsync(workspace, 0, ctrl, (cudaStream_t)stream) != cudaSuccess) return SANTA_ERR_CUDA;
+    return SANTA_OK;
+}
+
+int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, const void *v_cache,
+                 const int32_t *seq_lens, int32_t S, int32_t mode, uint64_t seed, float *out, int32_t *idx_out,
+                 void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if ((rc = check_mode_S(mode, S))) return rc;
+    if (!q || !k_cache || !v_cache || !seq_lens || !out) return SANTA_ERR_INVALID_ARG;
+    if (!workspace) return SANTA_ERR_WORKSPACE;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(seq_lens, 4) || (idx_out && !aligned(idx_out, 4)) || !aligned(workspace, 256))
+        return SANTA_ERR_MISALIGNED;
+    const bool dense = (mode == SANTA_DENSE);
+    const WsLayout wl = ws_layout(shape->B, shape->H_q, shape->H_kv, shape->d, shape->n_max, dense);
+    if (workspace_bytes < wl.total) return SANTA_ERR_WORKSPACE;
+    if (wl.ctrl + sizeof(int) * (CTRL_GROUPS + (size_t)shape->B * shape->H_kv) > 65536) return SANTA_ERR_UNSUPPORTED;
+
+    int dev, sms, optin;
+    if ((rc = device_info(&dev, &sms, &optin))) return rc;
+    const int D = shape->d, G = shape->H_q / shape->H_kv;
+    const int L = choose_L(shape, sms);
+    const int ns_used = (shape->n_max + L - 1) / L;
+
+    Params p{};
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.q = static_cast<const uint16_t *>(q);
+    p.k = static_cast<const uint16_t *>(k_cache);
+    p.v = static_cast<const uint16_t *>(v_cache);
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.idx_out = dense ? nullptr : idx_out;
+    p.ctrl = reinterpret_cast<int32_t *>(ws + wl.ctrl);
+    if (!dense) {
+        p.w = reinterpret_cast<float *>(ws + wl.w);
+        p.coff = reinterpret_cast<double *>(ws + wl.coff);
+        p.split_c = reinterpret_cast<int32_t *>(ws + wl.split_c);
+        p.split_W = reinterpret_cast<double *>(ws + wl.split_W);
+    } else {
+        p.dpart_o = reinterpret_cast<float *>(ws + wl.dpart_o);
+        p.dpart_ml = reinterpret_cast<float *>(ws + wl.dpart_ml);
+    }
+    p.B = shape->B;
+    p.H_q = shape->H_q;
+    p.H_kv = shape->H_kv;
+    p.n_max = shape->n_max;
+    p.n_pad = wl.n_pad;
+    p.nch = wl.nch;
+    p.ns_max = wl.ns_max;
+    p.L = L;
+    p.S = dense ? 1 : S;
+    p.mode = mode;
+    p.seed = seed;
+    p.rS = 1.0 / (double)p.S;
+    const float scale = shape->scale != 0.f ? shape->scale : (float)(1.0 / std::sqrt((double)D));
+    const double k2 = (double)scale * 1.4426950408889634;  // scale * log2(e)
+    p.k2_hi = (float)k2;
+    p.k2_lo = (float)(k2 - (double)p.k2_hi);
+    p.tau2 = (float)(2.0 * 1.4426950408889634);  // refine scores within e^-2 of the maximum
+    p.wait_ns = 2000000000ull;
+
+    const int kind = dense ? KIND_DENSE : KIND_SAMPLE;
+    const void *fn = (D == 128) ? kernel_d128(kind, G) : kernel_d64(kind, G);
+    if (!fn) return SANTA_ERR_UNSUPPORTED;
+    const int smem = dense ? dense_smem_bytes(D, G, shape->B)
+                           : sample_smem_bytes(D, G, shape->B, p.S, ns_used, mode);
+    if (smem > optin) return SANTA_ERR_UNSUPPORTED;
+    int occ = 0;
+    if ((rc = prepare_fn(fn, dev, smem, &occ))) return rc;
+    const long long items = (long long)shape->B * shape->H_kv * ns_used;
+    long long grid = (long long)sms * occ;
+    if (grid > items) grid = items;
+    if (grid < 1) grid = 1;
+    void *args[] = {&p};
+    if (cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(NT), args, (size_t)smem, (cudaStream_t)stream) !=
+        cudaSuccess)
+        return SANTA_ERR_CUDA;
+    return SANTA_OK;
+}
+
+int santa_sample_points(int32_t B, int32_t H_q, int32_t S, int32_t mode, uint64_t seed, double *t_out,
+                        void *stream)
+{
+    if (B < 1 || H_q < 1 || S < 1 || S > SMAX || !t_out) return SANTA_ERR_INVALID_ARG;
+    if (mode != SANTA_STRATIFIED && mode != SANTA_SYSTEMATIC && mode != SANTA_IID) return SANTA_ERR_INVALID_ARG;
+    if (!aligned(t_out, 8)) return SANTA_ERR_MISALIGNED;
+    const double rS = 1.0 / (double)S;
+    cudaError_t e;
+    if (mode == SANTA_IID) {
+        void *args[] = {&B, &H_q, &S, &seed, &t_out};
+        e = cudaLaunchKernel(points_iid_kernel(), dim3((unsigned)(B * H_q)), dim3(256), args, 0,
+                             (cudaStream_t)stream);
+    } else {
+        const size_t total = (size_t)B * H_q * S;
+        void *args[] = {&B, &H_q, &S, &mode, &seed, (void *)&rS, &t_out};
+        e = cudaLaunchKernel(points_kernel(), dim3((unsigned)((total + 255) / 256)), dim3(256), args, 0,
+                             (cudaStream_t)stream);
+    }
+    return e == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
+}
+
+int santa_device_status(void *workspace, int32_t *code, void *stream)
+{
+    if (!workspace || !code) return SANTA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return SANTA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SANTA_ERR_CUDA;
+    *code = v;
+    if (v != 0) {
+        if (cudaMemsetAsync(workspace, 0, sizeof v, s) != cudaSuccess) return SANTA_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return SANTA_ERR_CUDA;
+        return SANTA_ERR_DEVICE;
+    }
+    return SANTA_OK;
+}
+
+}  // extern "C"

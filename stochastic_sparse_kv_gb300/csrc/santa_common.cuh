@@ -1,0 +1,301 @@
+// santa_common.cuh -- device helpers and launch parameters shared by the SANTA kernels.
+//
+// Everything here serves the two persistent kernels of libsanta.so: the sampled path
+// (scores -> softmax CDF -> stratified/systematic points -> gather-add, "Stochastic
+// Sparse Attention for Memory-Bound Inference", abstract) and the dense split-K
+// baseline.  sm_103a only.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace santa {
+
+constexpr int NT = 256;              // threads per CTA
+constexpr int NWARP = NT / 32;       // 8 warps
+constexpr int LMAX = 1024;           // longest split (keys)
+constexpr int LMIN = 256;            // shortest split
+constexpr int CHUNK = 32;            // keys per CDF chunk (one 128-byte line of fp32 w)
+constexpr int NS_LIMIT = 512;        // most splits one sequence may have
+constexpr int BMAX = 1024;           // batch rows per call
+constexpr int SMAX = 4096;           // samples per (b, h)
+constexpr int TILE_BYTES = 16384;    // one staged K (or V) tile
+
+// Control block (int32 words at the start of the workspace).
+enum : int { CTRL_ERR = 0, CTRL_WORK = 1, CTRL_EXIT = 2, CTRL_GROUPS = 64 };
+constexpr int DEV_BAD_SEQLEN = 1;
+constexpr int DEV_TIMEOUT = 2;
+
+enum : int { MODE_DENSE = 0, MODE_STRATIFIED = 1, MODE_SYSTEMATIC = 2, MODE_IID = 3 };
+
+// Workspace carve-up (byte offsets, each 256-aligned).
+struct WsLayout {
+    size_t ctrl, w, coff, split_c, split_W, dpart_o, dpart_ml, total;
+    int n_pad, nch, ns_max;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline WsLayout ws_layout(int B, int H_q, int H_kv, int d, int n_max, bool dense)
+{
+    WsLayout L{};
+    L.n_pad = (int)align_up((size_t)n_max, CHUNK);
+    L.nch = L.n_pad / CHUNK;
+    L.ns_max = (n_max + LMIN - 1) / LMIN;
+    const size_t BH = (size_t)B * H_q;
+    size_t off = 0;
+    L.ctrl = off;
+    off = align_up(off + sizeof(int) * (CTRL_GROUPS + (size_t)B * H_kv), 256);
+    if (!dense) {
+        L.w = off;       off = align_up(off + BH * L.n_pad * sizeof(float), 256);
+        L.coff = off;    off = align_up(off + BH * L.nch * sizeof(double), 256);
+        L.split_c = off; off = align_up(off + BH * L.ns_max * sizeof(int), 256);
+        L.split_W = off; off = align_up(off + BH * L.ns_max * sizeof(double), 256);
+        L.dpart_o = L.dpart_ml = 0;
+    } else {
+        L.dpart_o = off;  off = align_up(off + BH * L.ns_max * d * sizeof(float), 256);
+        L.dpart_ml = off; off = align_up(off + BH * L.ns_max * 2 * sizeof(float), 256);
+        L.w = L.coff = L.split_c = L.split_W = 0;
+    }
+    L.total = off;
+    return L;
+}
+
+struct Params {
+    const uint16_t *q, *k, *v;   // bf16 bits
+    const int32_t *seq_lens;
+    float *out;
+    int32_t *idx_out;
+    int32_t *ctrl;
+    float *w;
+    double *coff;
+    int32_t *split_c;
+    double *split_W;
+    float *dpart_o, *dpart_ml;
+    int B, H_q, H_kv, n_max, n_pad, nch, ns_max;
+    int L;            // split length (keys), multiple of the tile size and of CHUNK
+    int S, mode;
+    uint64_t seed;
+    double rS;        // fp64 value nearest 1/S
+    float k2_hi, k2_lo;  // scale*log2(e) as an unevaluated fp32 sum
+    float tau2;       // refinement window (log2 units)
+    uint64_t wait_ns; // bounded-wait limit
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the barrier phase with the given parity; give up after limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completion counted on `bar` in bytes.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// ------------------------------------------------------------------ arithmetic
+
+// bf16 pair (low element in the low half) -> packed fp32 pair, exact.
+__device__ __forceinline__ unsigned long long bf16x2_to_f32x2(uint32_t w)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xffff0000u));
+    return r;
+}
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// acc += a * b on two fp32 lanes at once (Blackwell packed FMA).
+__device__ __forceinline__ void ffma2(unsigned long long &acc, unsigned long long a, unsigned long long b)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ unsigned long long fmul2(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ float f32x2_sum(unsigned long long x)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+    return __fadd_rn(lo, hi);
+}
+
+__device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float2 f32x2_unpack(unsigned long long x)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+    return make_float2(lo, hi);
+}
+
+// Error-free transformations (Knuth's TwoSum, Dekker's Fast2Sum, FMA-based TwoProd):
+// s + e == a + b exactly.  The _rn intrinsics keep the compiler from contracting or
+// reassociating them.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ void fast_two_sum(float a, float b, float &s, float &e)
+{
+    s = __fadd_rn(a, b);
+    e = __fsub_rn(b, __fsub_rn(s, a));
+}
+
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+// 1, 2, 3", SC'11): 10 rounds of two 64x64->128 multiplies, key bumped by the Weyl
+// constants between rounds.
+__device__ __forceinline__ void philox4x64_10(uint64_t c[4], uint64_t k0, uint64_t k1)
+{
+    const uint64_t M0 = 0xD2E7470EE14C6C93ULL, M1 = 0xCA5A826395121157ULL;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B97F4A7C15ULL;
+            k1 += 0xBB67AE8584CAA73BULL;
+        }
+        const uint64_t hi0 = __umul64hi(M0, c[0]), lo0 = M0 * c[0];
+        const uint64_t hi1 = __umul64hi(M1, c[2]), lo1 = M1 * c[2];
+        const uint64_t y0 = hi1 ^ c[1] ^ k0, y2 = hi0 ^ c[3] ^ k1;
+        c[0] = y0;
+        c[1] = lo1;
+        c[2] = y2;
+        c[3] = lo0;
+    }
+}
+
+// Top 32 bits of a Philox word, as an exact fp64 uniform in [0, 1).
+__device__ __forceinline__ double word_uniform(uint64_t x)
+{
+    return __dmul_rn(__uint2double_rn((uint32_t)(x >> 32)), 0x1p-32);
+}
+
+// Philox block (blk, b, h, domain) keyed by (seed, 0).
+__device__ __forceinline__ void philox_block(uint64_t seed, uint64_t blk, int b, int h, uint64_t dom,
+                                             uint64_t out[4])
+{
+    out[0] = blk;
+    out[1] = (uint64_t)b;
+    out[2] = (uint64_t)h;
+    out[3] = dom;
+    philox4x64_10(out, seed, 0);
+}
+
+// Sample point t_s of (b, h) for the systematic and stratified modes:
+//   systematic  t_s = (u + s) * rS, u from word 0 of block (0, b, h, 2)
+//   stratified  t_s = (s + u_s) * rS, u_s from word s%4 of block (s/4, b, h, 1)
+// with rS the fp64 value nearest 1/S; u + s is exact, the multiply rounds once.
+__device__ __forceinline__ double sample_point(int mode, uint64_t seed, int b, int h, int s, double rS)
+{
+    uint64_t rnd[4];
+    if (mode == MODE_SYSTEMATIC) {
+        philox_block(seed, 0, b, h, 2, rnd);
+        return __dmul_rn(__dadd_rn(word_uniform(rnd[0]), (double)s), rS);
+    }
+    philox_block(seed, (uint64_t)(s / 4), b, h, 1, rnd);
+    return __dmul_rn(__dadd_rn((double)s, word_uniform(rnd[s % 4])), rS);
+}
+
+// Non-negative fp64 values compare like their bit patterns as unsigned integers.
+__device__ __forceinline__ uint64_t dkey(double x) { return (uint64_t)__double_as_longlong(x); }
+
+// 2^e as an fp64 (0 below the normal range); e <= 0 here.
+__device__ __forceinline__ double pow2d(int e)
+{
+    return e < -1022 ? 0.0 : __longlong_as_double((long long)(1023 + e) << 52);
+}
+
+// 2^e as an fp64 for 0 <= e <= 1023.
+__device__ __forceinline__ double pow2pos(int e)
+{
+    return __longlong_as_double((long long)(1023 + e) << 52);
+}
+
+__device__ __forceinline__ void set_dev_error(int32_t *ctrl, int bits)
+{
+    atomicOr(ctrl + CTRL_ERR, bits);
+}
+
+}  // namespace santa

@@ -1,0 +1,21 @@
+// santa_kernels.h -- internal: kernel registry shared by the host API and the kernel
+// translation units (one per head dimension).
+#pragma once
+
+namespace santa {
+
+enum KernelKind : int { KIND_SAMPLE = 0, KIND_DENSE = 1 };
+
+// Kernel entry for (kind, G) at head dimension 64 or 128, or nullptr.
+const void *kernel_d64(int kind, int G);
+const void *kernel_d128(int kind, int G);
+
+// Sampled kernel's and dense kernel's dynamic shared-memory bytes.
+int sample_smem_bytes(int D, int G, int B, int S, int ns_used, int mode);
+int dense_smem_bytes(int D, int G, int B);
+
+// Device points kernel (santa_sample_points).
+const void *points_kernel();
+const void *points_iid_kernel();
+
+}  // namespace santa

@@ -1,0 +1,169 @@
+"""ctypes binding to libsanta.so (the C ABI in include/santa.h).
+
+Argument marshalling only: every step of the decode step runs in the library's CUDA
+kernels.  PyTorch provides device memory and streams.  If the library has not been built
+or cannot be loaded, every call raises -- there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsanta.so")
+
+OK = 0
+DENSE, STRATIFIED, SYSTEMATIC, IID = 0, 1, 2, 3
+MODES = {"dense": DENSE, "stratified": STRATIFIED, "systematic": SYSTEMATIC, "iid": IID}
+DEV_BAD_SEQLEN, DEV_TIMEOUT = 1, 2
+
+# every symbol include/santa.h declares
+EXPORTS = ("santa_workspace_size", "santa_workspace_init", "santa_decode", "santa_sample_points",
+           "santa_device_status", "santa_status_string", "santa_version")
+
+
+class SantaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("n_max", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libsanta.so (raises if it is missing: build it with __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libsanta.so not found at {p}; build it first (python -c "
+                               "'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(p)
+        vp, i32, u64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64, ctypes.c_size_t
+        lib.santa_workspace_size.argtypes = [ctypes.POINTER(Shape), i32, i32, ctypes.POINTER(sz)]
+        lib.santa_workspace_size.restype = ctypes.c_int
+        lib.santa_workspace_init.argtypes = [vp, sz, vp]
+        lib.santa_workspace_init.restype = ctypes.c_int
+        lib.santa_decode.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, vp, i32, i32, u64, vp, vp, vp, sz, vp]
+        lib.santa_decode.restype = ctypes.c_int
+        lib.santa_sample_points.argtypes = [i32, i32, i32, i32, u64, vp, vp]
+        lib.santa_sample_points.restype = ctypes.c_int
+        lib.santa_device_status.argtypes = [vp, ctypes.POINTER(i32), vp]
+        lib.santa_device_status.restype = ctypes.c_int
+        lib.santa_status_string.argtypes = [ctypes.c_int]
+        lib.santa_status_string.restype = ctypes.c_char_p
+        lib.santa_version.argtypes = []
+        lib.santa_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().santa_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise SantaError(rc, what)
+
+
+def _mode(mode) -> int:
+    return MODES[mode] if isinstance(mode, str) else int(mode)
+
+
+def make_shape(B, H_q, H_kv, d, n_max, scale: float = 0.0) -> Shape:
+    return Shape(int(B), int(H_q), int(H_kv), int(d), int(n_max), float(scale))
+
+
+def workspace_size(shape: Shape, S: int, mode) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().santa_workspace_size(ctypes.byref(shape), int(S), _mode(mode), ctypes.byref(n)),
+           "santa_workspace_size")
+    return int(n.value)
+
+
+def _stream_ptr(stream) -> int | None:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def new_workspace(nbytes: int, device, stream=None) -> torch.Tensor:
+    """A zero-initialised workspace (torch allocation, 256-byte aligned)."""
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    _check(load().santa_workspace_init(ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                       ctypes.c_void_p(_stream_ptr(stream))), "santa_workspace_init")
+    return ws
+
+
+_ws_cache: dict = {}
+
+
+def _cached_workspace(nbytes: int, device, stream) -> torch.Tensor:
+    key = (torch.device(device), _stream_ptr(stream))
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = new_workspace(nbytes, device, stream)
+        _ws_cache[key] = ws
+    return ws
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens: torch.Tensor,
+           S: int, mode="systematic", seed: int = 0, scale: float = 0.0, out: torch.Tensor | None = None,
+           idx_out: torch.Tensor | None = None, want_idx: bool = True, workspace: torch.Tensor | None = None,
+           stream=None):
+    """One SANTA (or dense) decode step on the GPU.  q [B,H_q,d], k/v [B,H_kv,n_max,d] bf16,
+    seq_lens [B] int32, all on one CUDA device.  Returns (out fp32 [B,H_q,d],
+    idx int32 [B,H_q,S] or None)."""
+    m = _mode(mode)
+    B, H_q, d = q.shape
+    _, H_kv, n_max, d2 = k_cache.shape
+    for t, name in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if seq_lens.dtype != torch.int32 or not seq_lens.is_cuda:
+        raise ValueError("seq_lens must be an int32 CUDA tensor")
+    if v_cache.shape != k_cache.shape or d2 != d:
+        raise ValueError("k_cache/v_cache/q shapes disagree")
+    shape = make_shape(B, H_q, H_kv, d, n_max, scale)
+    dev = q.device
+    if out is None:
+        out = torch.empty(B, H_q, d, dtype=torch.float32, device=dev)
+    if m != DENSE and want_idx and idx_out is None:
+        idx_out = torch.empty(B, H_q, S, dtype=torch.int32, device=dev)
+    nbytes = workspace_size(shape, S if m != DENSE else 1, m)
+    ws = workspace if workspace is not None else _cached_workspace(nbytes, dev, stream)
+    rc = load().santa_decode(ctypes.byref(shape), ctypes.c_void_p(q.data_ptr()),
+                             ctypes.c_void_p(k_cache.data_ptr()), ctypes.c_void_p(v_cache.data_ptr()),
+                             ctypes.c_void_p(seq_lens.data_ptr()), int(S), m, ctypes.c_uint64(seed),
+                             ctypes.c_void_p(out.data_ptr()),
+                             ctypes.c_void_p(idx_out.data_ptr() if (idx_out is not None and m != DENSE) else 0),
+                             ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.c_void_p(_stream_ptr(stream)))
+    _check(rc, "santa_decode")
+    return out, (idx_out if m != DENSE else None)
+
+
+def sample_points(B: int, H_q: int, S: int, mode, seed: int, device="cuda", stream=None) -> torch.Tensor:
+    t = torch.empty(B, H_q, S, dtype=torch.float64, device=device)
+    _check(load().santa_sample_points(int(B), int(H_q), int(S), _mode(mode), ctypes.c_uint64(seed),
+                                      ctypes.c_void_p(t.data_ptr()), ctypes.c_void_p(_stream_ptr(stream))),
+           "santa_sample_points")
+    return t
+
+
+def device_status(workspace: torch.Tensor, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    load().santa_device_status(ctypes.c_void_p(workspace.data_ptr()), ctypes.byref(code),
+                               ctypes.c_void_p(_stream_ptr(stream)))
+    return int(code.value)

@@ -1,0 +1,107 @@
+"""The C ABI of libsanta.so, checked without a GPU: the library loads, exports every
+symbol include/santa.h declares, sizes workspaces, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from stochastic_sparse_kv_gb300 import santa, _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return santa.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "santa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(santa_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(santa.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert santa.status_string(0) == "ok"
+    for rc in (-1, -2, -3, -4, -5, -6):
+        assert santa.status_string(rc) not in ("ok", "unknown status")
+    assert lib.santa_version() >= 10000
+
+
+def test_workspace_size_matches_layout(lib):
+    sh = santa.make_shape(16, 32, 8, 128, 32768)
+    n = santa.workspace_size(sh, 256, "systematic")
+    # w fp32 per (b, h_q, key) dominates: 16*32*32768*4 = 67 MB
+    assert 16 * 32 * 32768 * 4 < n < 16 * 32 * 32768 * 4 * 1.1
+    nd = santa.workspace_size(sh, 1, "dense")
+    assert nd > 16 * 32 * (32768 // 256) * 128 * 4
+    assert n % 256 == 0 and nd % 256 == 0
+
+
+@pytest.mark.parametrize("shape,S,mode,rc", [
+    ((16, 32, 8, 128, 32768), 256, 2, 0),
+    ((0, 32, 8, 128, 32768), 256, 2, -1),       # B < 1
+    ((1, 30, 8, 128, 1024), 256, 2, -1),        # H_q % H_kv != 0
+    ((1, 48, 3, 128, 1024), 256, 2, -4),        # G = 16 unsupported
+    ((1, 32, 8, 96, 1024), 256, 2, -4),         # d = 96 unsupported
+    ((1, 32, 8, 128, 1024), 0, 2, -1),          # S = 0
+    ((1, 32, 8, 128, 1024), 4097, 1, -1),       # S too large
+    ((1, 32, 8, 128, 1024), 0, 0, 0),           # dense ignores S
+    ((1, 32, 8, 128, 1024), 16, 7, -1),         # bad mode
+    ((1025, 32, 8, 128, 1024), 16, 2, -4),      # B > 1024
+    ((1, 32, 8, 128, 524289), 16, 2, -4),       # n_max too large
+])
+def test_workspace_size_validation(lib, shape, S, mode, rc):
+    sh = santa.make_shape(*shape)
+    n = ctypes.c_size_t(0)
+    assert lib.santa_workspace_size(ctypes.byref(sh), S, mode, ctypes.byref(n)) == rc
+
+
+def test_decode_rejects_bad_arguments_on_the_host(lib):
+    sh = santa.make_shape(1, 4, 1, 64, 256)
+    good = 4096  # a fake, 256-aligned address: never dereferenced, validation comes first
+    ws_n = santa.workspace_size(sh, 16, 2)
+    args = dict(q=good, k=good, v=good, sl=good, S=16, mode=2, out=good, idx=good, ws=good, wsn=ws_n)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return lib.santa_decode(ctypes.byref(sh), ctypes.c_void_p(a["q"]), ctypes.c_void_p(a["k"]),
+                                ctypes.c_void_p(a["v"]), ctypes.c_void_p(a["sl"]), a["S"], a["mode"],
+                                ctypes.c_uint64(0), ctypes.c_void_p(a["out"]), ctypes.c_void_p(a["idx"]),
+                                ctypes.c_void_p(a["ws"]), a["wsn"], None)
+
+    assert call(q=0) == -1
+    assert call(sl=0) == -1
+    assert call(out=0) == -1
+    assert call(ws=0) == -3
+    assert call(wsn=ws_n - 1) == -3
+    assert call(q=good + 8) == -2
+    assert call(ws=good + 16) == -2
+    assert call(S=0) == -1
+    assert call(mode=9) == -1
+    bad = santa.make_shape(1, 4, 3, 64, 256)
+    assert lib.santa_decode(ctypes.byref(bad), None, None, None, None, 16, 2, ctypes.c_uint64(0),
+                            None, None, None, 0, None) == -1
+    assert lib.santa_sample_points(0, 1, 1, 2, ctypes.c_uint64(0), ctypes.c_void_p(good), None) == -1
+    assert lib.santa_sample_points(1, 1, 1, 0, ctypes.c_uint64(0), ctypes.c_void_p(good), None) == -1
+
+
+def test_binding_refuses_to_run_without_the_library(tmp_path):
+    import importlib
+    mod = importlib.reload(santa)
+    try:
+        with pytest.raises(RuntimeError):
+            mod._lib = None
+            mod.load(str(tmp_path / "missing.so"))
+    finally:
+        importlib.reload(santa)
