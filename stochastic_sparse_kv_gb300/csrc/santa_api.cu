@@ -7,13 +7,20 @@
 
 #include "../../include/santa.h"
 #include "santa_dense.cuh"
+#include "santa_gather.cuh"
 #include "santa_kernels.h"
+#include "santa_score.cuh"
 
 namespace santa {
 
-int sample_smem_bytes(int D, int G, int B, int S, int ns_used, int mode)
+int score_smem_bytes(int D, int G, int B)
 {
-    return sample_smem(D, G, B, S, ns_used, mode).total;
+    return score_smem(D, G, B, SCORE_NSTAGE).total;
+}
+
+int gather_smem_bytes(int D, int S, int ns_used, int mode)
+{
+    return gather_smem(D, S, ns_used, mode).total;
 }
 
 int dense_smem_bytes(int D, int G, int B)
@@ -264,6 +271,7 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     if (!dense) {
         p.w = reinterpret_cast<float *>(ws + wl.w);
         p.coff = reinterpret_cast<double *>(ws + wl.coff);
+        p.cshift = reinterpret_cast<int32_t *>(ws + wl.cshift);
         p.split_c = reinterpret_cast<int32_t *>(ws + wl.split_c);
         p.split_W = reinterpret_cast<double *>(ws + wl.split_W);
     } else {
@@ -289,14 +297,22 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     p.tau2 = (float)(2.0 * 1.4426950408889634);  // refine scores within e^-2 of the maximum
     p.wait_ns = 2000000000ull;
 
-    const int kind = dense ? KIND_DENSE : KIND_SAMPLE;
+    const int kind = dense ? KIND_DENSE : KIND_SCORE;
     const void *fn = (D == 128) ? kernel_d128(kind, G) : kernel_d64(kind, G);
     if (!fn) return SANTA_ERR_UNSUPPORTED;
-    const int smem = dense ? dense_smem_bytes(D, G, shape->B)
-                           : sample_smem_bytes(D, G, shape->B, p.S, ns_used, mode);
+    const int smem = dense ? dense_smem_bytes(D, G, shape->B) : score_smem_bytes(D, G, shape->B);
     if (smem > optin) return SANTA_ERR_UNSUPPORTED;
     int occ = 0;
     if ((rc = prepare_fn(fn, dev, smem, &occ))) return rc;
+    const void *fn2 = nullptr;
+    int smem2 = 0;
+    if (!dense) {
+        fn2 = (D == 128) ? kernel_d128(KIND_GATHER, G) : kernel_d64(KIND_GATHER, G);
+        smem2 = gather_smem_bytes(D, p.S, ns_used, mode);
+        if (smem2 > optin) return SANTA_ERR_UNSUPPORTED;
+        int occ2 = 0;
+        if ((rc = prepare_fn(fn2, dev, smem2, &occ2))) return rc;
+    }
     const long long items = (long long)shape->B * shape->H_kv * ns_used;
     long long grid = (long long)sms * occ;
     if (grid > items) grid = items;
@@ -305,6 +321,20 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     if (cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(NT), args, (size_t)smem, (cudaStream_t)stream) !=
         cudaSuccess)
         return SANTA_ERR_CUDA;
+    if (!dense) {
+        // value stage: one CTA per (b, h_q), a programmatic dependent of the score kernel
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)(shape->B * shape->H_q));
+        cfg.blockDim = dim3(NT);
+        cfg.dynamicSmemBytes = (size_t)smem2;
+        cfg.stream = (cudaStream_t)stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelExC(&cfg, fn2, args) != cudaSuccess) return SANTA_ERR_CUDA;
+    }
     return SANTA_OK;
 }
 

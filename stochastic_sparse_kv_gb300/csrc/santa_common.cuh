@@ -31,7 +31,7 @@ enum : int { MODE_DENSE = 0, MODE_STRATIFIED = 1, MODE_SYSTEMATIC = 2, MODE_IID 
 
 // Workspace carve-up (byte offsets, each 256-aligned).
 struct WsLayout {
-    size_t ctrl, w, coff, split_c, split_W, dpart_o, dpart_ml, total;
+    size_t ctrl, w, coff, cshift, split_c, split_W, dpart_o, dpart_ml, total;
     int n_pad, nch, ns_max;
 };
 
@@ -50,13 +50,14 @@ __host__ __device__ inline WsLayout ws_layout(int B, int H_q, int H_kv, int d, i
     if (!dense) {
         L.w = off;       off = align_up(off + BH * L.n_pad * sizeof(float), 256);
         L.coff = off;    off = align_up(off + BH * L.nch * sizeof(double), 256);
+        L.cshift = off;  off = align_up(off + BH * L.nch * sizeof(int), 256);
         L.split_c = off; off = align_up(off + BH * L.ns_max * sizeof(int), 256);
         L.split_W = off; off = align_up(off + BH * L.ns_max * sizeof(double), 256);
         L.dpart_o = L.dpart_ml = 0;
     } else {
         L.dpart_o = off;  off = align_up(off + BH * L.ns_max * d * sizeof(float), 256);
         L.dpart_ml = off; off = align_up(off + BH * L.ns_max * 2 * sizeof(float), 256);
-        L.w = L.coff = L.split_c = L.split_W = 0;
+        L.w = L.coff = L.cshift = L.split_c = L.split_W = 0;
     }
     L.total = off;
     return L;
@@ -70,6 +71,7 @@ struct Params {
     int32_t *ctrl;
     float *w;
     double *coff;
+    int32_t *cshift;
     int32_t *split_c;
     double *split_W;
     float *dpart_o, *dpart_ml;

@@ -55,6 +55,17 @@ struct DenseCfg {
                 if (C::head_of(l, i) == h) return i;
         return 0;
     }
+    // both packed per head (lane in bits 0-7, slot above), evaluated by the compiler
+    __host__ __device__ static constexpr unsigned long long rep_table()
+    {
+        unsigned long long t = 0;
+        for (int h = 0; h < G; ++h)
+            t |= (unsigned long long)(rep_lane(h) | (rep_slot(h) << 5)) << (8 * h);
+        return t;
+    }
+    static constexpr unsigned long long REP = rep_table();
+    __host__ __device__ static constexpr int lane_of(int h) { return (int)((REP >> (8 * h)) & 31); }
+    __host__ __device__ static constexpr int slot_of(int h) { return (int)((REP >> (8 * h + 5)) & 7); }
 };
 
 template <int D, int G>
@@ -80,37 +91,7 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_dense_kernel(const
     float *mg_ml = mg_o + NWARP * G * D;
     const float NEG_INF = __int_as_float(0xff800000);
 
-    {
-        constexpr int PER = (BMAX + NT - 1) / NT;
-        int cnt[PER];
-        int local = 0;
-        bool bad = false;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int b = tid * PER + i;
-            cnt[i] = 0;
-            if (b < B) {
-                int n = p.seq_lens[b];
-                if (n < 0 || n > p.n_max) {
-                    bad = true;
-                    n = 0;
-                }
-                nb[b] = n;
-                cnt[i] = H_kv * (n > 0 ? (n + L - 1) / L : 1);
-                local += cnt[i];
-            }
-        }
-        if (bad && blockIdx.x == 0) set_dev_error(p.ctrl, DEV_BAD_SEQLEN);
-        int total;
-        int run = block_excl_scan(local, misc + MISC_SCAN, &total);
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int b = tid * PER + i;
-            if (b < B) prefix[b] = run;
-            run += cnt[i];
-        }
-        if (tid == 0) prefix[B] = total;
-    }
+    build_item_space(p, nb, prefix, misc);
     if (tid == 0) {
         for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
         mbar_fence_init();
@@ -225,7 +206,7 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_dense_kernel(const
         for (int i = 0; i < C::NV; ++i) wm[i] = s2[i];
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) {
-            if (C::same_heads(m)) {
+            if (C::SAME & (unsigned)m) {
 #pragma unroll
                 for (int i = 0; i < C::NV; ++i) wm[i] = fmaxf(wm[i], __shfl_xor_sync(0xffffffffu, wm[i], m));
             }
@@ -233,7 +214,7 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_dense_kernel(const
         float m_new[G], alpha[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const float mt = __shfl_sync(0xffffffffu, wm[DC::rep_slot(h)], DC::rep_lane(h));
+            const float mt = __shfl_sync(0xffffffffu, wm[DC::slot_of(h)], DC::lane_of(h));
             m_new[h] = fmaxf(m_w[h], mt);
             alpha[h] = (m_new[h] == NEG_INF) ? 1.f : exp2f(m_w[h] - m_new[h]);
             m_w[h] = m_new[h];
@@ -289,14 +270,14 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_dense_kernel(const
             for (int i = 0; i < C::NV; ++i) lsum[i] = l_l[i];
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
-                if (C::same_heads(m)) {
+                if (C::SAME & (unsigned)m) {
 #pragma unroll
                     for (int i = 0; i < C::NV; ++i) lsum[i] = __fadd_rn(lsum[i], __shfl_xor_sync(0xffffffffu, lsum[i], m));
                 }
             }
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const float lh = __shfl_sync(0xffffffffu, lsum[DC::rep_slot(h)], DC::rep_lane(h));
+                const float lh = __shfl_sync(0xffffffffu, lsum[DC::slot_of(h)], DC::lane_of(h));
                 if (lane == 0) {
                     mg_ml[(warp * G + h) * 2] = m_w[h];
                     mg_ml[(warp * G + h) * 2 + 1] = lh;

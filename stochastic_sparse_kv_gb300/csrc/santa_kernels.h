@@ -4,15 +4,17 @@
 
 namespace santa {
 
-enum KernelKind : int { KIND_SAMPLE = 0, KIND_DENSE = 1 };
+enum KernelKind : int { KIND_SCORE = 0, KIND_DENSE = 1, KIND_GATHER = 2 };
 
 // Kernel entry for (kind, G) at head dimension 64 or 128, or nullptr.
 const void *kernel_d64(int kind, int G);
 const void *kernel_d128(int kind, int G);
 
-// Sampled kernel's and dense kernel's dynamic shared-memory bytes.
-int sample_smem_bytes(int D, int G, int B, int S, int ns_used, int mode);
+// Dynamic shared-memory bytes of the score, value-stage and dense kernels.
+int score_smem_bytes(int D, int G, int B);
+int gather_smem_bytes(int D, int S, int ns_used, int mode);
 int dense_smem_bytes(int D, int G, int B);
+constexpr int SCORE_NSTAGE = 4;
 
 // Device points kernel (santa_sample_points).
 const void *points_kernel();

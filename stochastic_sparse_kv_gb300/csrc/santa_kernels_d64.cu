@@ -1,19 +1,22 @@
 // Kernel instantiations for head dimension 64.
 #include "santa_dense.cuh"
+#include "santa_gather.cuh"
 #include "santa_kernels.h"
+#include "santa_score.cuh"
 
 namespace santa {
 
 const void *kernel_d64(int kind, int G)
 {
-    if (kind == KIND_SAMPLE) {
+    if (kind == KIND_GATHER) return (const void *)santa_gather_kernel<64>;
+    if (kind == KIND_SCORE) {
         switch (G) {
-        case 1: return (const void *)santa_sample_kernel<64, 1>;
-        case 2: return (const void *)santa_sample_kernel<64, 2>;
-        case 4: return (const void *)santa_sample_kernel<64, 4>;
-        case 8: return (const void *)santa_sample_kernel<64, 8>;
+        case 1: return (const void *)santa_score_kernel<64, 1, SCORE_NSTAGE>;
+        case 2: return (const void *)santa_score_kernel<64, 2, SCORE_NSTAGE>;
+        case 4: return (const void *)santa_score_kernel<64, 4, SCORE_NSTAGE>;
+        case 8: return (const void *)santa_score_kernel<64, 8, SCORE_NSTAGE>;
         }
-    } else {
+    } else if (kind == KIND_DENSE) {
         switch (G) {
         case 1: return (const void *)santa_dense_kernel<64, 1>;
         case 2: return (const void *)santa_dense_kernel<64, 2>;
