@@ -41,10 +41,11 @@ __host__ __device__ inline ScoreSmem score_smem(int D, int G, int B, int nstage)
     s.bar = off; off += nstage * 8;
     s.desc = off; off = (int)align_up((size_t)off + nstage * 16, 16);
     s.qf = off; off += G * D * 4;
-    s.tmax = off; off += G * NWARP * 4;
+    s.tmax = off; off += G * NWARP * 4 + G * 4;  // warp maxima, then the shared estimate
     s.misc = off; off += 16 * 4;
     s.nb = off; off += (int)align_up((size_t)B * 4, 16);
     s.prefix = off; off += (int)align_up((size_t)(B + 1) * 4, 16);
+    off = (int)align_up((size_t)off, 16);
     s.sc = off; off += 2 * 2 * G * TK * 4;
     off = (int)align_up((size_t)off, 16);
     s.chk_tot = off; off += 2 * G * (LMAX / CHUNK) * 8;
@@ -145,33 +146,56 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
     Item fz_item{0, 0, 0, 0, 1};
     bool aborted = false;
     int it = 0;
+    // shared running maximum of the group's heads (other CTAs' splits), and what this
+    // CTA last published
+    float gbase[G], published[G];
+    float *gsm = tmax + G * NWARP;  // G floats after the warp maxima
+#pragma unroll
+    for (int h = 0; h < G; ++h) gbase[h] = published[h] = NEG_INF;
+    uint4 gload = make_uint4(0, 0, 0, 0);
 
-    // weights and exact chunk totals of the pending tile (all threads)
+    // weights and exact chunk totals of the pending tile: a thread takes 4 consecutive
+    // keys of one head, 8 threads a chunk
     auto tile_weights = [&]() {
         const float *hi_b = scb + pt_buf * 2 * G * TK;
         const float *lo_b = hi_b + G * TK;
         const size_t bh0 = (size_t)pt_item.b * H_q + (size_t)pt_item.g * G;
-        for (int e = tid; e < G * TK; e += NT) {
-            const int h = e / TK, key = e % TK;
+        for (int e = tid; e < G * TK / 4; e += NT) {
+            const int h = e / (TK / 4), key = (e % (TK / 4)) * 4;
             float rm = runmax[0];
 #pragma unroll
             for (int hh = 1; hh < G; ++hh) rm = (h == hh) ? runmax[hh] : rm;
             const int ct = (int)ceilf(fminf(fmaxf(rm, -16777216.f), 16777216.f));
-            float w = 0.f;
-            if (key < pt_rows) {
-                const float d = __fadd_rn(__fsub_rn(hi_b[h * TK + key], (float)ct), lo_b[h * TK + key]);
-                w = exp2f(d);
-                p.w[(bh0 + h) * p.n_pad + (size_t)pt_item.r * L + (size_t)pt_tile * TK + key] = w;
-            }
-            float s = w, er = 0.f, t;
+            const float cf = (float)ct;
+            const float4 hv = *reinterpret_cast<const float4 *>(hi_b + h * TK + key);
+            const float4 lv = *reinterpret_cast<const float4 *>(lo_b + h * TK + key);
+            const float hs[4] = {hv.x, hv.y, hv.z, hv.w}, ls[4] = {lv.x, lv.y, lv.z, lv.w};
+            float w[4];
 #pragma unroll
-            for (int m = 16; m >= 1; m >>= 1) {
+            for (int u = 0; u < 4; ++u)
+                w[u] = (key + u < pt_rows) ? exp2f(__fadd_rn(__fsub_rn(hs[u], cf), ls[u])) : 0.f;
+            float *dst = p.w + (bh0 + h) * p.n_pad + (size_t)pt_item.r * L + (size_t)pt_tile * TK + key;
+            if (key + 4 <= pt_rows) {
+                *reinterpret_cast<float4 *>(dst) = make_float4(w[0], w[1], w[2], w[3]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (key + u < pt_rows) dst[u] = w[u];
+            }
+            float s, er, t;
+            two_sum(w[0], w[1], s, er);
+            two_sum(s, w[2], s, t);
+            er = __fadd_rn(er, t);
+            two_sum(s, w[3], s, t);
+            er = __fadd_rn(er, t);
+#pragma unroll
+            for (int m = 4; m >= 1; m >>= 1) {
                 const float s2 = __shfl_xor_sync(0xffffffffu, s, m);
                 const float e2 = __shfl_xor_sync(0xffffffffu, er, m);
                 two_sum(s, s2, s, t);
                 er = __fadd_rn(__fadd_rn(er, e2), t);
             }
-            if (lane == 0) {
+            if ((lane & 7) == 0) {
                 const int k = pt_tile * CPT + key / CHUNK;
                 chk_tot[(pt_par * G + h) * NCH + k] = __dadd_rn((double)s, (double)er);
                 chk_exp[(pt_par * G + h) * NCH + k] = ct;
@@ -249,7 +273,26 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
         // everyone is done with the previous tile: refill its slot, fold its maxima in,
         // and retire the work that was waiting for this barrier
         if (tid == 0 && it > 0) produce((it - 1) % NSTAGE);
-        if (pt_ok) fold_tmax();
+        if (pt_ok) {
+            fold_tmax();
+#pragma unroll
+            for (int h = 0; h < G; ++h) gbase[h] = fmaxf(gbase[h], gsm[h]);
+            // publish a raised maximum of this CTA's split to the group's shared estimate
+            if (tid < G) {
+                float rm = runmax[0];
+#pragma unroll
+                for (int hh = 1; hh < G; ++hh) rm = (tid == hh) ? runmax[hh] : rm;
+                float pb = published[0];
+#pragma unroll
+                for (int hh = 1; hh < G; ++hh) pb = (tid == hh) ? published[hh] : pb;
+                if (rm > pb) {
+                    atomicMax(p.gest + (size_t)pt_item.b * H_q + (size_t)pt_item.g * G + tid, float_ord(rm));
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh)
+                        if (tid == hh) published[hh] = rm;
+                }
+            }
+        }
         retire_pending();
         const int4 dsc = sdesc[slot];
         if (dsc.x == DESC_END) break;
@@ -267,6 +310,8 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
 #pragma unroll
                 for (int i = 0; i < 8; ++i) qp[h][i] = bf16x2_to_f32x2(wv[i]);
                 runmax[h] = NEG_INF;
+                gbase[h] = NEG_INF;
+                published[h] = NEG_INF;
             }
             for (int i = tid; i < G * D / 2; i += NT) {
                 const uint32_t w2 = *reinterpret_cast<const uint32_t *>(qg + 2 * i);
@@ -276,6 +321,15 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
             __syncthreads();
         }
 
+        // the group's shared maximum: loaded now, used from the next tile on
+        const size_t gidx = (size_t)cur.b * H_q + (size_t)cur.g * G;
+        if (tid == 0) {
+            if constexpr (G == 4) {
+                gload = __ldcg(reinterpret_cast<const uint4 *>(p.gest + gidx));
+            } else {
+                gload.x = __ldcg(p.gest + gidx + (tile % G));
+            }
+        }
         // ---- scores of this tile: warp `warp` takes keys [warp*KW, warp*KW + KW)
         const int buf = it & 1;
         float *sc_hi = scb + buf * 2 * G * TK;
@@ -308,13 +362,22 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
                 for (int i = 0; i < C::NV; ++i) wm[i] = fmaxf(wm[i], __shfl_xor_sync(0xffffffffu, wm[i], m));
             }
         }
-        // recompute, error-free, the scores within tau2 of the running maximum
+        if ((lane & C::SAME) == 0) {
+#pragma unroll
+            for (int i = 0; i < C::NV; ++i) tmax[C::head_of(lane, i) * NWARP + warp] = wm[i];
+        }
+        if (tile == 0) {
+            // first tile of a split: base the window on the whole tile's maximum
+            __syncthreads();
+            fold_tmax();
+        }
+        // recompute, error-free, the scores within tau2 of the best known maximum
 #pragma unroll
         for (int i = 0; i < C::NV; ++i) {
             const int h = C::head_of(lane, i);
-            float rm = runmax[0];
+            float rm = fmaxf(runmax[0], gbase[0]);
 #pragma unroll
-            for (int hh = 1; hh < G; ++hh) rm = (h == hh) ? runmax[hh] : rm;
+            for (int hh = 1; hh < G; ++hh) rm = (h == hh) ? fmaxf(runmax[hh], gbase[hh]) : rm;
             const float thr = fmaxf(rm, wm[i]) - p.tau2;
             unsigned cand = __ballot_sync(0xffffffffu, own[i] && s2[i] >= thr);
             while (cand) {
@@ -330,9 +393,16 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
                 }
             }
         }
-        if ((lane & C::SAME) == 0) {
-#pragma unroll
-            for (int i = 0; i < C::NV; ++i) tmax[C::head_of(lane, i) * NWARP + warp] = wm[i];
+        if (tid == 0) {
+            if constexpr (G == 4) {
+                gsm[0] = ord_float(gload.x);
+                gsm[1] = ord_float(gload.y);
+                gsm[2] = ord_float(gload.z);
+                gsm[3] = ord_float(gload.w);
+            } else {
+                // other group sizes read one head's estimate per tile, round robin
+                gsm[tile % G] = ord_float(gload.x);
+            }
         }
         // this tile's weights are written next iteration (after the barrier)
         pt_ok = true;

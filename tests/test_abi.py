@@ -42,7 +42,7 @@ def test_workspace_size_matches_layout(lib):
     sh = santa.make_shape(16, 32, 8, 128, 32768)
     n = santa.workspace_size(sh, 256, "systematic")
     # w fp32 per (b, h_q, key) dominates: 16*32*32768*4 = 67 MB
-    assert 16 * 32 * 32768 * 4 < n < 16 * 32 * 32768 * 4 * 1.1
+    assert 16 * 32 * 32768 * 4 < n < 16 * 32 * 32768 * 4 * 1.2
     nd = santa.workspace_size(sh, 1, "dense")
     assert nd > 16 * 32 * (32768 // 256) * 128 * 4
     assert n % 256 == 0 and nd % 256 == 0
