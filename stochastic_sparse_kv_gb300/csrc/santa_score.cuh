@@ -160,8 +160,12 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
         const float *hi_b = scb + pt_buf * 2 * G * TK;
         const float *lo_b = hi_b + G * TK;
         const size_t bh0 = (size_t)pt_item.b * H_q + (size_t)pt_item.g * G;
-        for (int e = tid; e < G * TK / 4; e += NT) {
-            const int h = e / (TK / 4), key = (e % (TK / 4)) * 4;
+        // whole warps take part (the chunk reduction shuffles across all 32 lanes); lanes
+        // past the end contribute zero and store nothing
+        for (int e0 = warp * 32; e0 < G * TK / 4; e0 += NT) {
+            const int e = e0 + lane;
+            const bool act = e < G * TK / 4;
+            const int h = act ? e / (TK / 4) : 0, key = act ? (e % (TK / 4)) * 4 : 0;
             float rm = runmax[0];
 #pragma unroll
             for (int hh = 1; hh < G; ++hh) rm = (h == hh) ? runmax[hh] : rm;
@@ -173,14 +177,16 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
             float w[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                w[u] = (key + u < pt_rows) ? exp2f(__fadd_rn(__fsub_rn(hs[u], cf), ls[u])) : 0.f;
-            float *dst = p.w + (bh0 + h) * p.n_pad + (size_t)pt_item.r * L + (size_t)pt_tile * TK + key;
-            if (key + 4 <= pt_rows) {
-                *reinterpret_cast<float4 *>(dst) = make_float4(w[0], w[1], w[2], w[3]);
-            } else {
+                w[u] = (act && key + u < pt_rows) ? exp2f(__fadd_rn(__fsub_rn(hs[u], cf), ls[u])) : 0.f;
+            if (act) {
+                float *dst = p.w + (bh0 + h) * p.n_pad + (size_t)pt_item.r * L + (size_t)pt_tile * TK + key;
+                if (key + 4 <= pt_rows) {
+                    *reinterpret_cast<float4 *>(dst) = make_float4(w[0], w[1], w[2], w[3]);
+                } else {
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (key + u < pt_rows) dst[u] = w[u];
+                    for (int u = 0; u < 4; ++u)
+                        if (key + u < pt_rows) dst[u] = w[u];
+                }
             }
             float s, er, t;
             two_sum(w[0], w[1], s, er);
@@ -195,7 +201,7 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
                 two_sum(s, s2, s, t);
                 er = __fadd_rn(__fadd_rn(er, e2), t);
             }
-            if ((lane & 7) == 0) {
+            if (act && (lane & 7) == 0) {
                 const int k = pt_tile * CPT + key / CHUNK;
                 chk_tot[(pt_par * G + h) * NCH + k] = __dadd_rn((double)s, (double)er);
                 chk_exp[(pt_par * G + h) * NCH + k] = ct;
