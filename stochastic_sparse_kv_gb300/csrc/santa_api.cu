@@ -274,7 +274,6 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
         p.cshift = reinterpret_cast<int32_t *>(ws + wl.cshift);
         p.split_c = reinterpret_cast<int32_t *>(ws + wl.split_c);
         p.split_W = reinterpret_cast<double *>(ws + wl.split_W);
-        p.gest = reinterpret_cast<unsigned *>(ws + wl.gest);
     } else {
         p.dpart_o = reinterpret_cast<float *>(ws + wl.dpart_o);
         p.dpart_ml = reinterpret_cast<float *>(ws + wl.dpart_ml);

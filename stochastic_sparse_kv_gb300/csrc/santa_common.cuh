@@ -31,7 +31,7 @@ enum : int { MODE_DENSE = 0, MODE_STRATIFIED = 1, MODE_SYSTEMATIC = 2, MODE_IID 
 
 // Workspace carve-up (byte offsets, each 256-aligned).
 struct WsLayout {
-    size_t ctrl, w, coff, cshift, split_c, split_W, gest, dpart_o, dpart_ml, total;
+    size_t ctrl, w, coff, cshift, split_c, split_W, dpart_o, dpart_ml, total;
     int n_pad, nch, ns_max;
 };
 
@@ -53,12 +53,11 @@ __host__ __device__ inline WsLayout ws_layout(int B, int H_q, int H_kv, int d, i
         L.cshift = off;  off = align_up(off + BH * L.nch * sizeof(int), 256);
         L.split_c = off; off = align_up(off + BH * L.ns_max * sizeof(int), 256);
         L.split_W = off; off = align_up(off + BH * L.ns_max * sizeof(double), 256);
-        L.gest = off;    off = align_up(off + BH * sizeof(unsigned), 256);
         L.dpart_o = L.dpart_ml = 0;
     } else {
         L.dpart_o = off;  off = align_up(off + BH * L.ns_max * d * sizeof(float), 256);
         L.dpart_ml = off; off = align_up(off + BH * L.ns_max * 2 * sizeof(float), 256);
-        L.w = L.coff = L.cshift = L.split_c = L.split_W = L.gest = 0;
+        L.w = L.coff = L.cshift = L.split_c = L.split_W = 0;
     }
     L.total = off;
     return L;
@@ -75,7 +74,6 @@ struct Params {
     int32_t *cshift;
     int32_t *split_c;
     double *split_W;
-    unsigned *gest;   // per (b, h_q): running score maximum shared across CTAs (ordered encoding)
     float *dpart_o, *dpart_ml;
     int B, H_q, H_kv, n_max, n_pad, nch, ns_max;
     int L;            // split length (keys), multiple of the tile size and of CHUNK
@@ -295,20 +293,6 @@ __device__ __forceinline__ double pow2d(int e)
 __device__ __forceinline__ double pow2pos(int e)
 {
     return __longlong_as_double((long long)(1023 + e) << 52);
-}
-
-// Order-preserving map of fp32 to uint32 (0 is below every encoded value, so a zeroed
-// word means "no estimate yet").
-__device__ __forceinline__ unsigned float_ord(float f)
-{
-    const unsigned u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float ord_float(unsigned o)
-{
-    if (o == 0u) return __int_as_float(0xff800000);
-    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
 }
 
 __device__ __forceinline__ void set_dev_error(int32_t *ctrl, int bits)

@@ -276,7 +276,6 @@ __global__ void __launch_bounds__(NT) santa_gather_kernel(const Params p)
             p.out[(size_t)bh * D + i] = __fdiv_rn(sum, (float)S);
         }
     }
-    if (tid == 0) p.gest[bh] = 0u;  // the score kernel's shared maximum, cleared for the next call
 }
 
 }  // namespace santa

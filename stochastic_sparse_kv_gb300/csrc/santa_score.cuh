@@ -41,7 +41,7 @@ __host__ __device__ inline ScoreSmem score_smem(int D, int G, int B, int nstage)
     s.bar = off; off += nstage * 8;
     s.desc = off; off = (int)align_up((size_t)off + nstage * 16, 16);
     s.qf = off; off += G * D * 4;
-    s.tmax = off; off += G * NWARP * 4 + G * 4;  // warp maxima, then the shared estimate
+    s.tmax = off; off += G * NWARP * 4;
     s.misc = off; off += 16 * 4;
     s.nb = off; off += (int)align_up((size_t)B * 4, 16);
     s.prefix = off; off += (int)align_up((size_t)(B + 1) * 4, 16);
@@ -146,13 +146,6 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
     Item fz_item{0, 0, 0, 0, 1};
     bool aborted = false;
     int it = 0;
-    // shared running maximum of the group's heads (other CTAs' splits), and what this
-    // CTA last published
-    float gbase[G], published[G];
-    float *gsm = tmax + G * NWARP;  // G floats after the warp maxima
-#pragma unroll
-    for (int h = 0; h < G; ++h) gbase[h] = published[h] = NEG_INF;
-    uint4 gload = make_uint4(0, 0, 0, 0);
 
     // weights and exact chunk totals of the pending tile: a thread takes 4 consecutive
     // keys of one head, 8 threads a chunk
@@ -279,26 +272,7 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
         // everyone is done with the previous tile: refill its slot, fold its maxima in,
         // and retire the work that was waiting for this barrier
         if (tid == 0 && it > 0) produce((it - 1) % NSTAGE);
-        if (pt_ok) {
-            fold_tmax();
-#pragma unroll
-            for (int h = 0; h < G; ++h) gbase[h] = fmaxf(gbase[h], gsm[h]);
-            // publish a raised maximum of this CTA's split to the group's shared estimate
-            if (tid < G) {
-                float rm = runmax[0];
-#pragma unroll
-                for (int hh = 1; hh < G; ++hh) rm = (tid == hh) ? runmax[hh] : rm;
-                float pb = published[0];
-#pragma unroll
-                for (int hh = 1; hh < G; ++hh) pb = (tid == hh) ? published[hh] : pb;
-                if (rm > pb) {
-                    atomicMax(p.gest + (size_t)pt_item.b * H_q + (size_t)pt_item.g * G + tid, float_ord(rm));
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh)
-                        if (tid == hh) published[hh] = rm;
-                }
-            }
-        }
+        if (pt_ok) fold_tmax();
         retire_pending();
         const int4 dsc = sdesc[slot];
         if (dsc.x == DESC_END) break;
@@ -316,8 +290,6 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
 #pragma unroll
                 for (int i = 0; i < 8; ++i) qp[h][i] = bf16x2_to_f32x2(wv[i]);
                 runmax[h] = NEG_INF;
-                gbase[h] = NEG_INF;
-                published[h] = NEG_INF;
             }
             for (int i = tid; i < G * D / 2; i += NT) {
                 const uint32_t w2 = *reinterpret_cast<const uint32_t *>(qg + 2 * i);
@@ -327,15 +299,6 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
             __syncthreads();
         }
 
-        // the group's shared maximum: loaded now, used from the next tile on
-        const size_t gidx = (size_t)cur.b * H_q + (size_t)cur.g * G;
-        if (tid == 0) {
-            if constexpr (G == 4) {
-                gload = __ldcg(reinterpret_cast<const uint4 *>(p.gest + gidx));
-            } else {
-                gload.x = __ldcg(p.gest + gidx + (tile % G));
-            }
-        }
         // ---- scores of this tile: warp `warp` takes keys [warp*KW, warp*KW + KW)
         const int buf = it & 1;
         float *sc_hi = scb + buf * 2 * G * TK;
@@ -377,13 +340,13 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
             __syncthreads();
             fold_tmax();
         }
-        // recompute, error-free, the scores within tau2 of the best known maximum
+        // recompute, error-free, the scores within tau2 of the split's running maximum
 #pragma unroll
         for (int i = 0; i < C::NV; ++i) {
             const int h = C::head_of(lane, i);
-            float rm = fmaxf(runmax[0], gbase[0]);
+            float rm = runmax[0];
 #pragma unroll
-            for (int hh = 1; hh < G; ++hh) rm = (h == hh) ? fmaxf(runmax[hh], gbase[hh]) : rm;
+            for (int hh = 1; hh < G; ++hh) rm = (h == hh) ? runmax[hh] : rm;
             const float thr = fmaxf(rm, wm[i]) - p.tau2;
             unsigned cand = __ballot_sync(0xffffffffu, own[i] && s2[i] >= thr);
             while (cand) {
@@ -397,17 +360,6 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
                     sc_hi[hh * TK + key] = hi;
                     sc_lo[hh * TK + key] = lo;
                 }
-            }
-        }
-        if (tid == 0) {
-            if constexpr (G == 4) {
-                gsm[0] = ord_float(gload.x);
-                gsm[1] = ord_float(gload.y);
-                gsm[2] = ord_float(gload.z);
-                gsm[3] = ord_float(gload.w);
-            } else {
-                // other group sizes read one head's estimate per tile, round robin
-                gsm[tile % G] = ord_float(gload.x);
             }
         }
         // this tile's weights are written next iteration (after the barrier)
