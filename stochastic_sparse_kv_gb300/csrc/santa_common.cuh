@@ -280,6 +280,19 @@ __device__ __forceinline__ double sample_point(int mode, uint64_t seed, int b, i
     return __dmul_rn(__dadd_rn((double)s, word_uniform(rnd[s % 4])), rS);
 }
 
+// A non-negative fp32 value below 2^13, truncated to a multiple of 2^-50, as an integer
+// (bit manipulation only, exact for every value with no bits below 2^-50).
+__device__ __forceinline__ long long fixed50(float w)
+{
+    const uint32_t u = __float_as_uint(w);
+    const int ex = (int)((u >> 23) & 0xffu);
+    if (ex == 0) return 0;                     // zero (subnormals are far below 2^-50)
+    const unsigned long long m = (u & 0x7fffffu) | 0x800000u;  // w = m * 2^(ex - 150)
+    const int sh = ex - 100;                   // w * 2^50 = m * 2^(ex - 100)
+    if (sh >= 0) return (long long)(m << sh);
+    return sh > -24 ? (long long)(m >> (-sh)) : 0;
+}
+
 // Non-negative fp64 values compare like their bit patterns as unsigned integers.
 __device__ __forceinline__ uint64_t dkey(double x) { return (uint64_t)__double_as_longlong(x); }
 

@@ -10,7 +10,7 @@
 //   coff     fp64 exclusive prefix of the 32-key chunk totals within the split, in the
 //            split's scale 2^-c_r, and cshift = c_r - c_t of each chunk
 //   split_W  fp64 split total and split_c = c_r (the integer scale of the split)
-// Chunk totals are exact (double-float sums of the fp32 weights); all rescaling is by
+// Chunk totals are exact (64-bit fixed-point sums of the fp32 weights); rescaling is by
 // powers of two, so the CDF that the value stage assembles from these pieces has no
 // rounding beyond that of the fp32 weights themselves.
 //
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
     int *nb = reinterpret_cast<int *>(smem + lay.nb);
     int *prefix = reinterpret_cast<int *>(smem + lay.prefix);
     float *scb = reinterpret_cast<float *>(smem + lay.sc);  // [buf][hi|lo][G][TK]
-    double *chk_tot = reinterpret_cast<double *>(smem + lay.chk_tot);  // [parity][G][NCH]
+    long long *chk_tot = reinterpret_cast<long long *>(smem + lay.chk_tot);  // [parity][G][NCH]
     int *chk_exp = reinterpret_cast<int *>(smem + lay.chk_exp);        // [parity][G][NCH]
     const float NEG_INF = __int_as_float(0xff800000);
 
@@ -147,56 +147,31 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
     bool aborted = false;
     int it = 0;
 
-    // weights and exact chunk totals of the pending tile: a thread takes 4 consecutive
-    // keys of one head, 8 threads a chunk
+    // weights and exact chunk totals of the pending tile: one key per thread, a warp per
+    // 32-key chunk; the chunk total is an exact sum in 64-bit fixed point (2^-50 units of
+    // the chunk's scale 2^c_t; every weight is at most ~1, so 32 of them fit easily)
     auto tile_weights = [&]() {
         const float *hi_b = scb + pt_buf * 2 * G * TK;
         const float *lo_b = hi_b + G * TK;
         const size_t bh0 = (size_t)pt_item.b * H_q + (size_t)pt_item.g * G;
-        // whole warps take part (the chunk reduction shuffles across all 32 lanes); lanes
-        // past the end contribute zero and store nothing
-        for (int e0 = warp * 32; e0 < G * TK / 4; e0 += NT) {
+        for (int e0 = warp * 32; e0 < G * TK; e0 += NT) {  // whole warps (they shuffle)
             const int e = e0 + lane;
-            const bool act = e < G * TK / 4;
-            const int h = act ? e / (TK / 4) : 0, key = act ? (e % (TK / 4)) * 4 : 0;
+            const int h = e / TK, key = e % TK;
             float rm = runmax[0];
 #pragma unroll
             for (int hh = 1; hh < G; ++hh) rm = (h == hh) ? runmax[hh] : rm;
             const int ct = (int)ceilf(fminf(fmaxf(rm, -16777216.f), 16777216.f));
-            const float cf = (float)ct;
-            const float4 hv = *reinterpret_cast<const float4 *>(hi_b + h * TK + key);
-            const float4 lv = *reinterpret_cast<const float4 *>(lo_b + h * TK + key);
-            const float hs[4] = {hv.x, hv.y, hv.z, hv.w}, ls[4] = {lv.x, lv.y, lv.z, lv.w};
-            float w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                w[u] = (act && key + u < pt_rows) ? exp2f(__fadd_rn(__fsub_rn(hs[u], cf), ls[u])) : 0.f;
-            if (act) {
-                float *dst = p.w + (bh0 + h) * p.n_pad + (size_t)pt_item.r * L + (size_t)pt_tile * TK + key;
-                if (key + 4 <= pt_rows) {
-                    *reinterpret_cast<float4 *>(dst) = make_float4(w[0], w[1], w[2], w[3]);
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (key + u < pt_rows) dst[u] = w[u];
-                }
+            float w = 0.f;
+            if (key < pt_rows) {
+                w = exp2f(__fadd_rn(__fsub_rn(hi_b[h * TK + key], (float)ct), lo_b[h * TK + key]));
+                p.w[(bh0 + h) * p.n_pad + (size_t)pt_item.r * L + (size_t)pt_tile * TK + key] = w;
             }
-            float s, er, t;
-            two_sum(w[0], w[1], s, er);
-            two_sum(s, w[2], s, t);
-            er = __fadd_rn(er, t);
-            two_sum(s, w[3], s, t);
-            er = __fadd_rn(er, t);
+            long long v = fixed50(w);
 #pragma unroll
-            for (int m = 4; m >= 1; m >>= 1) {
-                const float s2 = __shfl_xor_sync(0xffffffffu, s, m);
-                const float e2 = __shfl_xor_sync(0xffffffffu, er, m);
-                two_sum(s, s2, s, t);
-                er = __fadd_rn(__fadd_rn(er, e2), t);
-            }
-            if (act && (lane & 7) == 0) {
+            for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+            if (lane == 0) {
                 const int k = pt_tile * CPT + key / CHUNK;
-                chk_tot[(pt_par * G + h) * NCH + k] = __dadd_rn((double)s, (double)er);
+                chk_tot[(pt_par * G + h) * NCH + k] = v;
                 chk_exp[(pt_par * G + h) * NCH + k] = ct;
             }
         }
@@ -210,7 +185,7 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_score_kernel(const
             double tot = 0.0;
             int ce = INT_MIN;
             if (lane < nchunks) {
-                tot = chk_tot[(fz_par * G + h) * NCH + lane];
+                tot = __dmul_rn(__ll2double_rn(chk_tot[(fz_par * G + h) * NCH + lane]), 0x1p-50);
                 ce = chk_exp[(fz_par * G + h) * NCH + lane];
             }
             int cr = ce;

@@ -41,12 +41,13 @@ _lib = None
 
 
 def load(path: str | None = None):
-    """Load libsanta.so (raises if it is missing: build it with __graft_entry__.build())."""
+    """Load libsanta.so (raises if it is missing: build it with __graft_entry__.build()).
+    The SANTA_LIBRARY environment variable, if set, names another build to load."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        p = path or LIB_PATH
+        p = path or os.environ.get("SANTA_LIBRARY", LIB_PATH)
         if not os.path.exists(p):
             raise RuntimeError(f"libsanta.so not found at {p}; build it first (python -c "
                                "'import __graft_entry__ as g; g.build()')")
