@@ -28,9 +28,13 @@ sys.path.insert(0, ROOT)
 METRIC = "SANTA decode-attn µs/step @32k ctx, B=16, S=256; achieved HBM GB/s vs dense"
 UNIT = "us/step"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "santa_sample_kernel_b16_32k_traffic.txt")
-KERNEL_SOURCES = ["stochastic_sparse_kv_gb300/csrc/santa_common.cuh", "stochastic_sparse_kv_gb300/csrc/santa_sample.cuh",
-                  "stochastic_sparse_kv_gb300/csrc/santa_api.cu"]
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "santa_decode_b16_32k_traffic.txt")
+CSRC = os.path.join("stochastic_sparse_kv_gb300", "csrc")
+KERNEL_SOURCES = [os.path.join(CSRC, f) for f in ("santa_common.cuh", "santa_sample.cuh", "santa_score.cuh",
+                                                   "santa_gather.cuh", "santa_dense.cuh", "santa_api.cu")]
+# The sampled path is two launches chained by programmatic dependent launch (the value
+# stage overlaps the score kernel's tail), so one santa_decode call is timed as the unit.
+ROOFLINE_UNIT = "santa_decode: santa_score_kernel<128,4> + santa_gather_kernel<128> (PDL-chained)"
 
 
 def log(*a):
@@ -269,11 +273,11 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
-                         "kernel": "santa_sample_kernel<128,4>", "algorithmic_bytes_per_launch": abytes,
+                         "kernel": ROOFLINE_UNIT, "algorithmic_bytes_per_launch": abytes,
                          "avg_launch_us": round(avg_launch_ms * 1000, 2)},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (1 if mode == "dense" else 2),
             "clocks": clocks,
             "modes": modes,
             "S_sweep_systematic": sweep,
