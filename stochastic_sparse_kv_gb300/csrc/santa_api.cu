@@ -15,7 +15,7 @@ namespace santa {
 
 int score_smem_bytes(int D, int G, int B)
 {
-    return score_smem(D, G, B, SCORE_NSTAGE).total;
+    return score_smem(D, G, B).total;
 }
 
 int gather_smem_bytes(int D, int S, int ns_used, int mode)
@@ -169,13 +169,32 @@ int check_mode_S(int32_t mode, int32_t S)
     return SANTA_OK;
 }
 
-// Split length: the longest of 1024/512/256 keys that still gives every SM at least
-// four work items, and at most NS_LIMIT splits per sequence.
-int choose_L(const santa_shape *sh, int sms)
+// Split length of the sampled path: the longest of 512/256/128 keys that gives every
+// warp of the persistent score kernel (NWARP per SM) at least eight splits, so that the
+// dynamic schedule ends evenly; at most NS_LIMIT splits per sequence.
+int choose_L_sampled(const santa_shape *sh, int sms)
+{
+    const int cand[3] = {512, 256, 128};
+    const long long groups = (long long)sh->B * sh->H_kv;
+    int L = LMIN;
+    for (int i = 0; i < 3; ++i) {
+        const long long ns = (sh->n_max + cand[i] - 1) / cand[i];
+        if (groups * ns >= 8LL * NWARP * sms) {
+            L = cand[i];
+            break;
+        }
+    }
+    while ((sh->n_max + L - 1) / L > NS_LIMIT && L < LMAX) L *= 2;
+    return L;
+}
+
+// Split length of the dense kernel (CTA-wide 64-key tiles): the longest of 1024/512/256
+// keys that still gives every SM at least four work items.
+int choose_L_dense(const santa_shape *sh, int sms)
 {
     const int cand[3] = {1024, 512, 256};
     const long long groups = (long long)sh->B * sh->H_kv;
-    int L = LMIN;
+    int L = 256;
     for (int i = 0; i < 3; ++i) {
         const long long ns = (sh->n_max + cand[i] - 1) / cand[i];
         if (groups * ns >= 4LL * sms) {
@@ -256,7 +275,7 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     int dev, sms, optin;
     if ((rc = device_info(&dev, &sms, &optin))) return rc;
     const int D = shape->d, G = shape->H_q / shape->H_kv;
-    const int L = choose_L(shape, sms);
+    const int L = dense ? choose_L_dense(shape, sms) : choose_L_sampled(shape, sms);
     const int ns_used = (shape->n_max + L - 1) / L;
 
     Params p{};
@@ -270,10 +289,12 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     p.ctrl = reinterpret_cast<int32_t *>(ws + wl.ctrl);
     if (!dense) {
         p.w = reinterpret_cast<float *>(ws + wl.w);
+        p.cmax = reinterpret_cast<float *>(ws + wl.cmax);
         p.coff = reinterpret_cast<double *>(ws + wl.coff);
         p.cshift = reinterpret_cast<int32_t *>(ws + wl.cshift);
         p.split_c = reinterpret_cast<int32_t *>(ws + wl.split_c);
         p.split_W = reinterpret_cast<double *>(ws + wl.split_W);
+        p.split_m = reinterpret_cast<float *>(ws + wl.split_m);
     } else {
         p.dpart_o = reinterpret_cast<float *>(ws + wl.dpart_o);
         p.dpart_ml = reinterpret_cast<float *>(ws + wl.dpart_ml);
@@ -294,7 +315,7 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     const double k2 = (double)scale * 1.4426950408889634;  // scale * log2(e)
     p.k2_hi = (float)k2;
     p.k2_lo = (float)(k2 - (double)p.k2_hi);
-    p.tau2 = (float)(2.0 * 1.4426950408889634);  // refine scores within e^-2 of the maximum
+    p.tau2 = (float)(3.0 * 1.4426950408889634);  // re-score keys within e^-3 of the maximum
     p.wait_ns = 2000000000ull;
 
     const int kind = dense ? KIND_DENSE : KIND_SCORE;

@@ -1,9 +1,11 @@
-// santa_common.cuh -- device helpers and launch parameters shared by the SANTA kernels.
+// santa_common.cuh -- device helpers, constants and launch parameters shared by the
+// SANTA kernels.
 //
-// Everything here serves the two persistent kernels of libsanta.so: the sampled path
-// (scores -> softmax CDF -> stratified/systematic points -> gather-add, "Stochastic
-// Sparse Attention for Memory-Bound Inference", abstract) and the dense split-K
-// baseline.  sm_103a only.
+// Everything here serves the kernels of libsanta.so: the sampled path (a streaming
+// score kernel that leaves softmax weights and CDF pieces in the workspace, then a
+// value-stage kernel that draws stratified/systematic points, searches the CDF and
+// gather-adds V rows; "Stochastic Sparse Attention for Memory-Bound Inference",
+// abstract) and the dense split-K baseline.  sm_103a only.
 #pragma once
 
 #include <cstddef>
@@ -14,10 +16,11 @@ namespace santa {
 
 constexpr int NT = 256;              // threads per CTA
 constexpr int NWARP = NT / 32;       // 8 warps
-constexpr int LMAX = 1024;           // longest split (keys)
-constexpr int LMIN = 256;            // shortest split
+constexpr int LMAX = 512;            // longest split of the sampled path (keys)
+constexpr int LMIN = 128;            // shortest split (either path)
 constexpr int CHUNK = 32;            // keys per CDF chunk (one 128-byte line of fp32 w)
-constexpr int NS_LIMIT = 512;        // most splits one sequence may have
+constexpr int CPS_MAX = LMAX / CHUNK;  // chunks per split, at most (16)
+constexpr int NS_LIMIT = 1024;       // most splits one sequence may have
 constexpr int BMAX = 1024;           // batch rows per call
 constexpr int SMAX = 4096;           // samples per (b, h)
 constexpr int TILE_BYTES = 16384;    // one staged K (or V) tile
@@ -31,7 +34,7 @@ enum : int { MODE_DENSE = 0, MODE_STRATIFIED = 1, MODE_SYSTEMATIC = 2, MODE_IID 
 
 // Workspace carve-up (byte offsets, each 256-aligned).
 struct WsLayout {
-    size_t ctrl, w, coff, cshift, split_c, split_W, dpart_o, dpart_ml, total;
+    size_t ctrl, w, cmax, coff, cshift, split_c, split_W, split_m, dpart_o, dpart_ml, total;
     int n_pad, nch, ns_max;
 };
 
@@ -49,15 +52,17 @@ __host__ __device__ inline WsLayout ws_layout(int B, int H_q, int H_kv, int d, i
     off = align_up(off + sizeof(int) * (CTRL_GROUPS + (size_t)B * H_kv), 256);
     if (!dense) {
         L.w = off;       off = align_up(off + BH * L.n_pad * sizeof(float), 256);
+        L.cmax = off;    off = align_up(off + BH * L.nch * sizeof(float), 256);
         L.coff = off;    off = align_up(off + BH * L.nch * sizeof(double), 256);
         L.cshift = off;  off = align_up(off + BH * L.nch * sizeof(int), 256);
         L.split_c = off; off = align_up(off + BH * L.ns_max * sizeof(int), 256);
         L.split_W = off; off = align_up(off + BH * L.ns_max * sizeof(double), 256);
+        L.split_m = off; off = align_up(off + BH * L.ns_max * sizeof(float), 256);
         L.dpart_o = L.dpart_ml = 0;
     } else {
         L.dpart_o = off;  off = align_up(off + BH * L.ns_max * d * sizeof(float), 256);
         L.dpart_ml = off; off = align_up(off + BH * L.ns_max * 2 * sizeof(float), 256);
-        L.w = L.coff = L.cshift = L.split_c = L.split_W = 0;
+        L.w = L.cmax = L.coff = L.cshift = L.split_c = L.split_W = L.split_m = 0;
     }
     L.total = off;
     return L;
@@ -69,11 +74,13 @@ struct Params {
     float *out;
     int32_t *idx_out;
     int32_t *ctrl;
-    float *w;
-    double *coff;
-    int32_t *cshift;
-    int32_t *split_c;
-    double *split_W;
+    float *w;         // [B*H_q][n_pad] fp32 weights 2^(s log2e - c_t), c_t the chunk's scale
+    float *cmax;      // [B*H_q][nch] chunk maximum of s log2e (fast fp32 scores)
+    double *coff;     // [B*H_q][nch] exclusive prefix of chunk totals within the split (scale 2^-c_r)
+    int32_t *cshift;  // [B*H_q][nch] c_r - c_t
+    int32_t *split_c; // [B*H_q][ns_max] c_r, the split's integer scale
+    double *split_W;  // [B*H_q][ns_max] split total in scale 2^-c_r
+    float *split_m;   // [B*H_q][ns_max] split maximum of s log2e
     float *dpart_o, *dpart_ml;
     int B, H_q, H_kv, n_max, n_pad, nch, ns_max;
     int L;            // split length (keys), multiple of the tile size and of CHUNK
@@ -81,7 +88,7 @@ struct Params {
     uint64_t seed;
     double rS;        // fp64 value nearest 1/S
     float k2_hi, k2_lo;  // scale*log2(e) as an unevaluated fp32 sum
-    float tau2;       // refinement window (log2 units)
+    float tau2;       // re-scoring window below the maximum (log2 units)
     uint64_t wait_ns; // bounded-wait limit
 };
 
@@ -292,6 +299,15 @@ __device__ __forceinline__ long long fixed50(float w)
     if (sh >= 0) return (long long)(m << sh);
     return sh > -24 ? (long long)(m >> (-sh)) : 0;
 }
+
+// fp32 -> int32 key with the same order (negative values: all bits but the sign flipped),
+// for integer atomics on floats; and its inverse.
+__device__ __forceinline__ int fkey(float x)
+{
+    const int i = __float_as_int(x);
+    return i >= 0 ? i : (i ^ 0x7fffffff);
+}
+__device__ __forceinline__ float fkey_inv(int k) { return __int_as_float(k >= 0 ? k : (k ^ 0x7fffffff)); }
 
 // Non-negative fp64 values compare like their bit patterns as unsigned integers.
 __device__ __forceinline__ uint64_t dkey(double x) { return (uint64_t)__double_as_longlong(x); }

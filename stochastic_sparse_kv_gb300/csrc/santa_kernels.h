@@ -14,7 +14,6 @@ const void *kernel_d128(int kind, int G);
 int score_smem_bytes(int D, int G, int B);
 int gather_smem_bytes(int D, int S, int ns_used, int mode);
 int dense_smem_bytes(int D, int G, int B);
-constexpr int SCORE_NSTAGE = 4;
 
 // Device points kernel (santa_sample_points).
 const void *points_kernel();

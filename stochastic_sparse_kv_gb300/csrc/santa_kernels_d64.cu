@@ -11,10 +11,10 @@ const void *kernel_d64(int kind, int G)
     if (kind == KIND_GATHER) return (const void *)santa_gather_kernel<64>;
     if (kind == KIND_SCORE) {
         switch (G) {
-        case 1: return (const void *)santa_score_kernel<64, 1, SCORE_NSTAGE>;
-        case 2: return (const void *)santa_score_kernel<64, 2, SCORE_NSTAGE>;
-        case 4: return (const void *)santa_score_kernel<64, 4, SCORE_NSTAGE>;
-        case 8: return (const void *)santa_score_kernel<64, 8, SCORE_NSTAGE>;
+        case 1: return (const void *)santa_score_kernel<64, 1>;
+        case 2: return (const void *)santa_score_kernel<64, 2>;
+        case 4: return (const void *)santa_score_kernel<64, 4>;
+        case 8: return (const void *)santa_score_kernel<64, 8>;
         }
     } else if (kind == KIND_DENSE) {
         switch (G) {
