@@ -18,9 +18,9 @@ int score_smem_bytes(int D, int G, int B)
     return score_smem(D, G, B).total;
 }
 
-int gather_smem_bytes(int D, int S, int ns_used, int mode)
+int gather_smem_bytes(int D, int S, int nch_used, int mode)
 {
-    return gather_smem(D, S, ns_used, mode).total;
+    return gather_smem(D, S, nch_used, mode).total;
 }
 
 int dense_smem_bytes(int D, int G, int B)
@@ -158,7 +158,7 @@ int check_shape(const santa_shape *sh)
     if (G != 1 && G != 2 && G != 4 && G != 8) return SANTA_ERR_UNSUPPORTED;
     if (sh->d != 64 && sh->d != 128) return SANTA_ERR_UNSUPPORTED;
     if (sh->B > BMAX || sh->H_q > 1024) return SANTA_ERR_UNSUPPORTED;
-    if ((long long)sh->n_max > (long long)NS_LIMIT * LMAX) return SANTA_ERR_UNSUPPORTED;
+    if (sh->n_max > NMAX_LIMIT) return SANTA_ERR_UNSUPPORTED;
     return SANTA_OK;
 }
 
@@ -167,25 +167,6 @@ int check_mode_S(int32_t mode, int32_t S)
     if (mode < SANTA_DENSE || mode > SANTA_IID) return SANTA_ERR_INVALID_ARG;
     if (mode != SANTA_DENSE && (S < 1 || S > SMAX)) return SANTA_ERR_INVALID_ARG;
     return SANTA_OK;
-}
-
-// Split length of the sampled path: the longest of 512/256/128 keys that gives every
-// warp of the persistent score kernel (NWARP per SM) at least eight splits, so that the
-// dynamic schedule ends evenly; at most NS_LIMIT splits per sequence.
-int choose_L_sampled(const santa_shape *sh, int sms)
-{
-    const int cand[3] = {512, 256, 128};
-    const long long groups = (long long)sh->B * sh->H_kv;
-    int L = LMIN;
-    for (int i = 0; i < 3; ++i) {
-        const long long ns = (sh->n_max + cand[i] - 1) / cand[i];
-        if (groups * ns >= 8LL * NWARP * sms) {
-            L = cand[i];
-            break;
-        }
-    }
-    while ((sh->n_max + L - 1) / L > NS_LIMIT && L < LMAX) L *= 2;
-    return L;
 }
 
 // Split length of the dense kernel (CTA-wide 64-key tiles): the longest of 1024/512/256
@@ -275,8 +256,7 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     int dev, sms, optin;
     if ((rc = device_info(&dev, &sms, &optin))) return rc;
     const int D = shape->d, G = shape->H_q / shape->H_kv;
-    const int L = dense ? choose_L_dense(shape, sms) : choose_L_sampled(shape, sms);
-    const int ns_used = (shape->n_max + L - 1) / L;
+    const int L = dense ? choose_L_dense(shape, sms) : UNIT_KEYS;
 
     Params p{};
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -289,12 +269,10 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     p.ctrl = reinterpret_cast<int32_t *>(ws + wl.ctrl);
     if (!dense) {
         p.w = reinterpret_cast<float *>(ws + wl.w);
+        p.ctot = reinterpret_cast<float *>(ws + wl.ctot);
+        p.cexp = reinterpret_cast<int32_t *>(ws + wl.cexp);
         p.cmax = reinterpret_cast<float *>(ws + wl.cmax);
-        p.coff = reinterpret_cast<double *>(ws + wl.coff);
-        p.cshift = reinterpret_cast<int32_t *>(ws + wl.cshift);
-        p.split_c = reinterpret_cast<int32_t *>(ws + wl.split_c);
-        p.split_W = reinterpret_cast<double *>(ws + wl.split_W);
-        p.split_m = reinterpret_cast<float *>(ws + wl.split_m);
+        p.cpre = reinterpret_cast<uint64_t *>(ws + wl.cpre);
     } else {
         p.dpart_o = reinterpret_cast<float *>(ws + wl.dpart_o);
         p.dpart_ml = reinterpret_cast<float *>(ws + wl.dpart_ml);
@@ -329,12 +307,12 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     int smem2 = 0;
     if (!dense) {
         fn2 = (D == 128) ? kernel_d128(KIND_GATHER, G) : kernel_d64(KIND_GATHER, G);
-        smem2 = gather_smem_bytes(D, p.S, ns_used, mode);
+        smem2 = gather_smem_bytes(D, p.S, p.nch, mode);
         if (smem2 > optin) return SANTA_ERR_UNSUPPORTED;
         int occ2 = 0;
         if ((rc = prepare_fn(fn2, dev, smem2, &occ2))) return rc;
     }
-    const long long items = (long long)shape->B * shape->H_kv * ns_used;
+    const long long items = (long long)shape->B * shape->H_kv * ((shape->n_max + L - 1) / L);
     long long grid = (long long)sms * occ;
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;

@@ -16,11 +16,11 @@ namespace santa {
 
 constexpr int NT = 256;              // threads per CTA
 constexpr int NWARP = NT / 32;       // 8 warps
-constexpr int LMAX = 512;            // longest split of the sampled path (keys)
-constexpr int LMIN = 128;            // shortest split (either path)
+constexpr int UNIT_KEYS = 128;       // keys per work unit of the sampled path's score kernel
+constexpr int LMIN = 128;            // shortest split of the dense kernel
 constexpr int CHUNK = 32;            // keys per CDF chunk (one 128-byte line of fp32 w)
-constexpr int CPS_MAX = LMAX / CHUNK;  // chunks per split, at most (16)
-constexpr int NS_LIMIT = 1024;       // most splits one sequence may have
+constexpr int NS_LIMIT = 1024;       // most dense splits one sequence may have
+constexpr int NMAX_LIMIT = 524288;   // longest KV cache (keys)
 constexpr int BMAX = 1024;           // batch rows per call
 constexpr int SMAX = 4096;           // samples per (b, h)
 constexpr int TILE_BYTES = 16384;    // one staged K (or V) tile
@@ -34,7 +34,7 @@ enum : int { MODE_DENSE = 0, MODE_STRATIFIED = 1, MODE_SYSTEMATIC = 2, MODE_IID 
 
 // Workspace carve-up (byte offsets, each 256-aligned).
 struct WsLayout {
-    size_t ctrl, w, cmax, coff, cshift, split_c, split_W, split_m, dpart_o, dpart_ml, total;
+    size_t ctrl, w, ctot, cexp, cmax, cpre, dpart_o, dpart_ml, total;
     int n_pad, nch, ns_max;
 };
 
@@ -51,18 +51,16 @@ __host__ __device__ inline WsLayout ws_layout(int B, int H_q, int H_kv, int d, i
     L.ctrl = off;
     off = align_up(off + sizeof(int) * (CTRL_GROUPS + (size_t)B * H_kv), 256);
     if (!dense) {
-        L.w = off;       off = align_up(off + BH * L.n_pad * sizeof(float), 256);
-        L.cmax = off;    off = align_up(off + BH * L.nch * sizeof(float), 256);
-        L.coff = off;    off = align_up(off + BH * L.nch * sizeof(double), 256);
-        L.cshift = off;  off = align_up(off + BH * L.nch * sizeof(int), 256);
-        L.split_c = off; off = align_up(off + BH * L.ns_max * sizeof(int), 256);
-        L.split_W = off; off = align_up(off + BH * L.ns_max * sizeof(double), 256);
-        L.split_m = off; off = align_up(off + BH * L.ns_max * sizeof(float), 256);
+        L.w = off;    off = align_up(off + BH * L.n_pad * sizeof(float), 256);
+        L.ctot = off; off = align_up(off + BH * L.nch * sizeof(float), 256);
+        L.cexp = off; off = align_up(off + BH * L.nch * sizeof(int), 256);
+        L.cmax = off; off = align_up(off + BH * L.nch * sizeof(float), 256);
+        L.cpre = off; off = align_up(off + BH * L.nch * sizeof(uint64_t), 256);
         L.dpart_o = L.dpart_ml = 0;
     } else {
         L.dpart_o = off;  off = align_up(off + BH * L.ns_max * d * sizeof(float), 256);
         L.dpart_ml = off; off = align_up(off + BH * L.ns_max * 2 * sizeof(float), 256);
-        L.w = L.cmax = L.coff = L.cshift = L.split_c = L.split_W = L.split_m = 0;
+        L.w = L.ctot = L.cexp = L.cmax = L.cpre = 0;
     }
     L.total = off;
     return L;
@@ -75,15 +73,13 @@ struct Params {
     int32_t *idx_out;
     int32_t *ctrl;
     float *w;         // [B*H_q][n_pad] fp32 weights 2^(s log2e - c_t), c_t the chunk's scale
-    float *cmax;      // [B*H_q][nch] chunk maximum of s log2e (fast fp32 scores)
-    double *coff;     // [B*H_q][nch] exclusive prefix of chunk totals within the split (scale 2^-c_r)
-    int32_t *cshift;  // [B*H_q][nch] c_r - c_t
-    int32_t *split_c; // [B*H_q][ns_max] c_r, the split's integer scale
-    double *split_W;  // [B*H_q][ns_max] split total in scale 2^-c_r
-    float *split_m;   // [B*H_q][ns_max] split maximum of s log2e
+    float *ctot;      // [B*H_q][nch] chunk totals of w (chunk scale)
+    int32_t *cexp;    // [B*H_q][nch] c_t = ceil of the chunk's maximum of s log2e
+    float *cmax;      // [B*H_q][nch] the chunk's maximum of s log2e (fast fp32 scores)
+    uint64_t *cpre;   // [B*H_q][nch] value stage: fixed-point CDF prefix (very long sequences)
     float *dpart_o, *dpart_ml;
     int B, H_q, H_kv, n_max, n_pad, nch, ns_max;
-    int L;            // split length (keys), multiple of the tile size and of CHUNK
+    int L;            // keys per work unit (sampled path) or split length (dense), multiple of 64
     int S, mode;
     uint64_t seed;
     double rS;        // fp64 value nearest 1/S
@@ -168,6 +164,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// The same without an L2 eviction hint (data other warps re-read).
+__device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 // ------------------------------------------------------------------ arithmetic
@@ -287,21 +292,57 @@ __device__ __forceinline__ double sample_point(int mode, uint64_t seed, int b, i
     return __dmul_rn(__dadd_rn((double)s, word_uniform(rnd[s % 4])), rS);
 }
 
-// A non-negative fp32 value below 2^13, truncated to a multiple of 2^-50, as an integer
-// (bit manipulation only, exact for every value with no bits below 2^-50).
-__device__ __forceinline__ long long fixed50(float w)
+// ------------------------------------------------------------------ CDF fixed point
+//
+// The CDF pieces are unsigned 64-bit fixed-point numbers with FIX_F fraction bits in a
+// power-of-two scale: a chunk total t (fp32, scale 2^-c_t) enters its split (scale
+// 2^-c_r, c_r >= c_t) as round(t * 2^(FIX_F + c_t - c_r)).  Sums of these integers are
+// exact and order-independent, so patches by integer atomics stay deterministic, and
+// no fp64 arithmetic (slow on this part) is needed anywhere on the path.  Chunk totals
+// are at most 32 (weights <= 1), split totals at most 512 * 2^40 = 2^49, and a
+// sequence's total in the global scale at most 2^19 * 2^40 = 2^59.
+constexpr int FIX_F = 40;
+
+// round(x * 2^e) for a non-negative fp32 x (NaN and Inf are treated as 0).  The
+// result must stay below 2^64: here x * 2^e <= 2^49 always.
+__device__ __forceinline__ uint64_t fixp(float x, int e)
 {
-    const uint32_t u = __float_as_uint(w);
+    const uint32_t u = __float_as_uint(x);
     const int ex = (int)((u >> 23) & 0xffu);
-    if (ex == 0) return 0;                     // zero (subnormals are far below 2^-50)
-    const unsigned long long m = (u & 0x7fffffu) | 0x800000u;  // w = m * 2^(ex - 150)
-    const int sh = ex - 100;                   // w * 2^50 = m * 2^(ex - 100)
-    if (sh >= 0) return (long long)(m << sh);
-    return sh > -24 ? (long long)(m >> (-sh)) : 0;
+    if (ex == 0 || ex == 0xff || (u >> 31)) return 0;  // zero, subnormal, Inf/NaN, negative
+    const uint64_t m = (u & 0x7fffffu) | 0x800000u;     // x = m * 2^(ex - 150)
+    const int sh = ex - 150 + e;
+    if (sh >= 0) return sh < 40 ? (m << sh) : 0;       // (cannot happen for totals <= 2^9)
+    if (sh < -25) return 0;
+    return (m + (1ull << (-sh - 1))) >> (-sh);
+}
+
+// d << k, saturating at 2^64 - 1 (0 <= k).
+__device__ __forceinline__ uint64_t shl_sat(uint64_t d, int k)
+{
+    if (k == 0) return d;
+    if (k >= 64) return d ? ~0ull : 0ull;
+    return (d >> (64 - k)) ? ~0ull : (d << k);
+}
+
+// round(d / 2^k) (0 <= k); 0 for k >= 64.
+__device__ __forceinline__ uint64_t shr_round(uint64_t d, int k)
+{
+    if (k == 0) return d;
+    if (k >= 64) return 0;
+    return (d >> k) + ((d >> (k - 1)) & 1ull);
+}
+
+// 2^e as an fp32 for any integer e (0 below the normal range, +Inf above it).
+__device__ __forceinline__ float exp2i(int e)
+{
+    if (e < -126) return 0.f;
+    if (e > 127) return __int_as_float(0x7f800000);
+    return __int_as_float((e + 127) << 23);
 }
 
 // fp32 -> int32 key with the same order (negative values: all bits but the sign flipped),
-// for integer atomics on floats; and its inverse.
+// for integer reductions and atomics on floats; and its inverse.
 __device__ __forceinline__ int fkey(float x)
 {
     const int i = __float_as_int(x);
@@ -311,18 +352,6 @@ __device__ __forceinline__ float fkey_inv(int k) { return __int_as_float(k >= 0 
 
 // Non-negative fp64 values compare like their bit patterns as unsigned integers.
 __device__ __forceinline__ uint64_t dkey(double x) { return (uint64_t)__double_as_longlong(x); }
-
-// 2^e as an fp64 (0 below the normal range); e <= 0 here.
-__device__ __forceinline__ double pow2d(int e)
-{
-    return e < -1022 ? 0.0 : __longlong_as_double((long long)(1023 + e) << 52);
-}
-
-// 2^e as an fp64 for 0 <= e <= 1023.
-__device__ __forceinline__ double pow2pos(int e)
-{
-    return __longlong_as_double((long long)(1023 + e) << 52);
-}
 
 __device__ __forceinline__ void set_dev_error(int32_t *ctrl, int bits)
 {

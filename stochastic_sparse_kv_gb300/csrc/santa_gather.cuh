@@ -3,49 +3,64 @@
 // "Stochastic Sparse Attention for Memory-Bound Inference" (abstract): sample S << n_k
 // indices from the post-softmax distribution and aggregate only those value rows,
 // scaled by 1/S.  One CTA per (batch row b, query head h), launched as a programmatic
-// dependent of the score kernel (its point generation overlaps the score kernel's
-// tail).  It
-//   1. draws the S sorted points t_s (systematic, stratified, or sorted iid);
-//   2. re-scores error-free the keys within tau2 (log2 units) of the head's global
-//      maximum score -- found through the split and chunk maxima the score kernel
-//      left -- and patches their weights, the chunk offsets after them and the split
-//      totals (the heaviest keys' fp32 dot-product rounding would otherwise shift every
-//      later CDF boundary);
-//   3. merges the split totals exactly: O_r = sum_{r'<r} W_r' 2^(c_r' - C), Z = O_ns;
-//   4. maps each point to i_s = min{ j : W_j > t_s Z } by a split -> chunk -> key
-//      search, one thread per point with independent loads;
-//   5. gather-adds each distinct sampled V row once, weighted by its count, and
-//      writes out = sum / S and the sorted indices.
+// dependent of the score kernel (its point generation can overlap the score kernel's
+// tail).  The score kernel left, per 32-key chunk, the fp32 weights w_j in the chunk's
+// scale 2^-c_t, the chunk total, c_t and the chunk's maximum score.  After the
+// dependency wait the work is a few wide phases, each at most one round trip to memory,
+// in integer or fp32 arithmetic only:
+//   A. chunk data -> shared memory (left in global memory for very long sequences); the
+//      maximum score M and the largest scale C over the sequence;
+//   B. each chunk total as 64-bit fixed point in the global scale 2^-C,
+//      G_c = round(tot_c 2^(FIX_F + c_t - C)); hot chunks: maximum >= M - tau2 (at most
+//      HCAP: when more qualify, a histogram of the maxima keeps the hottest);
+//   C. heavy keys: keys of hot chunks whose score is >= M - tau2 (read off their weights);
+//   D. one thread per heavy key re-scores it error-free, rewrites its weight and adds the
+//      fixed-point change to its chunk's G_c (integer atomics: exact, in any order).  The
+//      heaviest keys' fp32 dot-product rounding would otherwise shift every later CDF
+//      boundary;
+//   E. the exact exclusive prefix O_c of the G_c (block scan), Z = the total;
+//   F. one thread per point: T = t Z, i = min{ j : W_j > T } by chunk -> key;
+//   G. each warp takes S/8 consecutive (sorted) points, loads each distinct V row once
+//      and adds it times its count; out = sum / S.
 #pragma once
 
 #include "santa_sample.cuh"
 
 namespace santa {
 
+constexpr int NCH_SMEM = 4096;  // a head's chunk arrays stay in shared memory up to this many chunks
+constexpr int HCAP = 128;       // hot chunks re-scored per head, at most
+constexpr int HBINS = 256;      // histogram bins that pick the hottest HCAP chunks
+constexpr int HKCAP = 512;      // heavy keys re-scored per head, at most
+
 struct GatherSmem {
-    int t, O, cr, sm, hot, idx, lead, acc, qf, misc, total;
+    int t, O, tot, ce, cm, hot, hv, hvw, hist, idx, acc, qf, misc, total;
 };
 
-__host__ __device__ inline GatherSmem gather_smem(int D, int S, int ns_used, int mode)
+__host__ __device__ inline GatherSmem gather_smem(int D, int S, int nch_used, int mode)
 {
     GatherSmem s{};
     const int Sp = (mode == MODE_IID) ? next_pow2(S) : S;
+    const int ncs = nch_used <= NCH_SMEM ? nch_used : 0;
     int off = 0;
     s.t = off; off += S * 8;
-    s.O = off; off += (ns_used + 1) * 8;
-    s.cr = off; off = (int)align_up((size_t)off + ns_used * 4, 16);
-    s.sm = off; off = (int)align_up((size_t)off + ns_used * 4, 16);
-    s.hot = off; off = (int)align_up((size_t)off + ns_used * 4, 16);
+    s.O = off; off += ncs * 8;
+    s.tot = off; off = (int)align_up((size_t)off + ncs * 4, 16);
+    s.ce = off; off = (int)align_up((size_t)off + ncs * 4, 16);
+    s.cm = off; off = (int)align_up((size_t)off + ncs * 4, 16);
+    s.hot = off; off = (int)align_up((size_t)off + HCAP * 4, 16);
+    s.hv = off; off = (int)align_up((size_t)off + HKCAP * 4, 16);
+    s.hvw = off; off = (int)align_up((size_t)off + HKCAP * 4, 16);
+    s.hist = off; off = (int)align_up((size_t)off + HBINS * 4, 16);
     s.idx = off; off = (int)align_up((size_t)off + Sp * 4, 16);
-    s.lead = off; off = (int)align_up((size_t)off + (S + 1) * 4, 16);
     s.acc = off; off += NWARP * D * 4;
     s.qf = off; off += D * 4;
-    s.misc = off; off += 16 * 4;
+    s.misc = off; off += 32 * 4;
     s.total = (int)align_up((size_t)off, 128);
     return s;
 }
 
-enum : int { GM_CMAX = 13, GM_NHOT = 14, GM_MAX = 15 };
+enum : int { GM_MAX = 0, GM_CMAX = 1, GM_NHOT = 2, GM_NHV = 3, GM_CNT = 4, GM_SCAN = 8 /* NWARP+1 words */ };
 
 template <int D>
 __global__ void __launch_bounds__(NT) santa_gather_kernel(const Params p)
@@ -54,7 +69,7 @@ __global__ void __launch_bounds__(NT) santa_gather_kernel(const Params p)
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned FULL = 0xffffffffu;
-    const int H_q = p.H_q, G = p.H_q / p.H_kv, L = p.L, S = p.S;
+    const int H_q = p.H_q, G = p.H_q / p.H_kv, S = p.S;
     const int bh = blockIdx.x;
     const int b = bh / H_q, h = bh % H_q, g = h / G;
     int n = p.seq_lens[b];
@@ -65,23 +80,28 @@ __global__ void __launch_bounds__(NT) santa_gather_kernel(const Params p)
             for (int i = tid; i < S; i += NT) p.idx_out[(size_t)bh * S + i] = -1;
         return;
     }
-    const int ns = (n + L - 1) / L;
-    const int ns_used = (p.n_max + L - 1) / L;
-    const int cps = L / CHUNK;  // chunks per full split
-    const GatherSmem lay = gather_smem(D, S, ns_used, p.mode);
-    double *tpt = reinterpret_cast<double *>(smem + lay.t);
-    double *O = reinterpret_cast<double *>(smem + lay.O);
-    int *crs = reinterpret_cast<int *>(smem + lay.cr);
-    float *smx = reinterpret_cast<float *>(smem + lay.sm);
+    const int nchn = (n + CHUNK - 1) / CHUNK;  // chunks of this sequence
+    const GatherSmem lay = gather_smem(D, S, p.nch, p.mode);
+    const bool in_smem = p.nch <= NCH_SMEM;
+    const size_t bhc = (size_t)bh * p.nch;
+    uint64_t *tfx = reinterpret_cast<uint64_t *>(smem + lay.t);  // points as 64-bit fractions
+    // the head's chunk arrays: shared-memory copies, or the workspace itself
+    uint64_t *O = in_smem ? reinterpret_cast<uint64_t *>(smem + lay.O) : p.cpre + bhc;
+    const float *ctot = in_smem ? reinterpret_cast<const float *>(smem + lay.tot) : p.ctot + bhc;
+    const int *cexp = in_smem ? reinterpret_cast<const int *>(smem + lay.ce) : p.cexp + bhc;
+    const float *cmx = in_smem ? reinterpret_cast<const float *>(smem + lay.cm) : p.cmax + bhc;
     int *hot = reinterpret_cast<int *>(smem + lay.hot);
+    int *hv = reinterpret_cast<int *>(smem + lay.hv);
+    float *hvw = reinterpret_cast<float *>(smem + lay.hvw);
+    int *hist = reinterpret_cast<int *>(smem + lay.hist);
     int *idx = reinterpret_cast<int *>(smem + lay.idx);
-    int *lead = reinterpret_cast<int *>(smem + lay.lead);
     float *acc_s = reinterpret_cast<float *>(smem + lay.acc);
     float *qf = reinterpret_cast<float *>(smem + lay.qf);
     int *misc = reinterpret_cast<int *>(smem + lay.misc);
+    uint64_t *scan64 = reinterpret_cast<uint64_t *>(misc + GM_SCAN);
     const int Sp = (p.mode == MODE_IID) ? next_pow2(S) : S;
 
-    // ---- 1. points (independent of the scores) and the query head in fp32
+    // ---- 0. points (independent of the scores) and the query head in fp32
     if (p.mode == MODE_IID) {
         unsigned *uk = reinterpret_cast<unsigned *>(idx);
         for (int s = tid; s < Sp; s += NT) {
@@ -109,141 +129,187 @@ __global__ void __launch_bounds__(NT) santa_gather_kernel(const Params p)
                 }
                 __syncthreads();
             }
-        for (int s = tid; s < S; s += NT) tpt[s] = __dmul_rn(__uint2double_rn(uk[s]), 0x1p-32);
+        for (int s = tid; s < S; s += NT) tfx[s] = (uint64_t)uk[s] << 32;  // u = x 2^-32 exactly
     } else {
-        for (int s = tid; s < S; s += NT) tpt[s] = sample_point(p.mode, p.seed, b, h, s, p.rS);
+        // the fp64 point as a 64-bit fraction (t < 1; the scaling by 2^64 is exact)
+        for (int s = tid; s < S; s += NT)
+            tfx[s] = __double2ull_rz(__dmul_rn(sample_point(p.mode, p.seed, b, h, s, p.rS), 0x1p64));
     }
     for (int i = tid; i < D; i += NT) qf[i] = __uint_as_float((uint32_t)p.q[(size_t)bh * D + i] << 16);
     if (tid == 0) {
-        misc[GM_NHOT] = 0;
         misc[GM_MAX] = INT_MIN;  // below the key of every fp32 value
+        misc[GM_CMAX] = INT_MIN;
+        misc[GM_NHOT] = 0;
+        misc[GM_NHV] = 0;
+        misc[GM_CNT] = 0;
     }
 
     pdl_wait();  // the score kernel's results are complete and visible from here on
-
-    // ---- 2. split data; the head's maximum score
-    const size_t bhs = (size_t)bh * p.ns_max;
     __syncthreads();
-    float mloc = __int_as_float(0xff800000);
-    for (int r = tid; r < ns; r += NT) {
-        crs[r] = __ldcg(p.split_c + bhs + r);
-        O[r] = __ldcg(p.split_W + bhs + r);
-        smx[r] = __ldcg(p.split_m + bhs + r);
-        mloc = fmaxf(mloc, smx[r]);
+
+    // ---- A. chunk data; the maximum score M and the largest chunk scale C
+    int mk = INT_MIN, cml = INT_MIN;
+    if (in_smem) {
+        float *tot_s = reinterpret_cast<float *>(smem + lay.tot);
+        int *ce_s = reinterpret_cast<int *>(smem + lay.ce);
+        float *cm_s = reinterpret_cast<float *>(smem + lay.cm);
+        for (int c = tid; c < nchn; c += NT) {
+            const float t = __ldcg(p.ctot + bhc + c);
+            const int e = __ldcg(p.cexp + bhc + c);
+            const float m = __ldcg(p.cmax + bhc + c);
+            tot_s[c] = t;
+            ce_s[c] = e;
+            cm_s[c] = m;
+            mk = max(mk, fkey(m));
+            cml = max(cml, e);
+        }
+    } else {
+        for (int c = tid; c < nchn; c += NT) {
+            mk = max(mk, fkey(__ldcg(p.cmax + bhc + c)));
+            cml = max(cml, __ldcg(p.cexp + bhc + c));
+        }
     }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(FULL, mloc, m));
-    if (lane == 0) atomicMax(misc + GM_MAX, fkey(mloc));
+    mk = __reduce_max_sync(FULL, mk);
+    cml = __reduce_max_sync(FULL, cml);
+    if (lane == 0) {
+        atomicMax(misc + GM_MAX, mk);
+        atomicMax(misc + GM_CMAX, cml);
+    }
     __syncthreads();
     const float M = fkey_inv(misc[GM_MAX]);
-    const float thr = M - p.tau2;
-    for (int r = tid; r < ns; r += NT)
-        if (smx[r] >= thr) hot[atomicAdd(misc + GM_NHOT, 1)] = r;
-    __syncthreads();
-
-    // ---- 3. re-score the keys within tau2 of the maximum; patch w, coff, W_r
-    const int nhot = misc[GM_NHOT];
-    const size_t bhc = (size_t)bh * p.nch;
-    float *wrow = p.w + (size_t)bh * p.n_pad;
-    const uint16_t *kg = p.k + ((size_t)b * p.H_kv + g) * (size_t)p.n_max * D;
-    for (int hi = warp; hi < nhot; hi += NWARP) {
-        const int r = hot[hi];
-        const int nck = (min(L, n - r * L) + CHUNK - 1) / CHUNK;
-        const size_t cbase = bhc + (size_t)r * cps;
-        const bool cact = lane < nck;
-        const float cm = cact ? __ldcg(p.cmax + cbase + lane) : __int_as_float(0xff800000);
-        const int csh = cact ? __ldcg(p.cshift + cbase + lane) : 0;
-        unsigned hm = __ballot_sync(FULL, cact && cm >= thr);
-        const int cr = crs[r];
-        double dlane = 0.0, dtot = 0.0;
-        while (hm) {
-            const int c = __ffs(hm) - 1;
-            hm &= hm - 1;
-            const int ct = cr - __shfl_sync(FULL, csh, c);
-            const int j0 = r * L + c * CHUNK;
-            const int jn = min(CHUNK, n - j0);
-            const float wv = lane < jn ? __ldcg(wrow + j0 + lane) : 0.f;
-            const float wthr = exp2f(thr - (float)ct);
-            unsigned heavy = __ballot_sync(FULL, lane < jn && wv >= wthr);
-            double dch = 0.0;
-            while (heavy) {
-                const int k = __ffs(heavy) - 1;
-                heavy &= heavy - 1;
-                float shi, slo;
-                refine_score<D>(reinterpret_cast<const uint8_t *>(kg + (size_t)(j0 + k) * D), qf, lane, p.k2_hi,
-                                p.k2_lo, shi, slo);
-                const float wnew = exp2f(__fadd_rn(__fsub_rn(shi, (float)ct), slo));
-                const float wold = __shfl_sync(FULL, wv, k);
-                if (lane == 0) wrow[j0 + k] = wnew;
-                dch = __dadd_rn(dch, __dsub_rn((double)wnew, (double)wold));
-            }
-            const double dsp = __dmul_rn(dch, pow2d(ct - cr));
-            if (lane > c) dlane = __dadd_rn(dlane, dsp);
-            dtot = __dadd_rn(dtot, dsp);
-        }
-        if (lane < nck && dlane != 0.0) p.coff[cbase + lane] = __dadd_rn(__ldcg(p.coff + cbase + lane), dlane);
-        if (lane == 0) O[r] = __dadd_rn(O[r], dtot);
-    }
-    __syncthreads();
-
-    // ---- 4. split offsets O_r = sum_{r' < r} W_r' 2^(c_r' - C) (exact scaling, fp64 sums)
-    if (warp == 0) {
-        int cm = INT_MIN;
-        for (int r = lane; r < ns; r += 32) cm = max(cm, crs[r]);
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) cm = max(cm, __shfl_xor_sync(FULL, cm, m));
-        double carry = 0.0;
-        for (int base = 0; base < ns; base += 32) {
-            const int r = base + lane;
-            const double x = r < ns ? __dmul_rn(O[r], pow2d(crs[r] - cm)) : 0.0;
-            double incl = x;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(FULL, incl, o);
-                if (lane >= o) incl = __dadd_rn(incl, y);
-            }
-            __syncwarp();
-            if (r < ns) O[r] = __dadd_rn(carry, __dsub_rn(incl, x));
-            carry = __dadd_rn(carry, __shfl_sync(FULL, incl, 31));
-        }
-        if (lane == 0) {
-            O[ns] = carry;  // Z, in the scale 2^-C
-            misc[GM_CMAX] = cm;
-        }
-    }
-    __syncthreads();
     const int Cm = misc[GM_CMAX];
-    const double Z = O[ns];
+    const float thr = M - p.tau2;  // keys with a score >= thr are re-scored
 
-    // ---- 5. points -> split (smem) -> chunk (coff, one line) -> key (w, one line)
-    for (int s = tid; s < S; s += NT) {
-        const double T = __dmul_rn(tpt[s], Z);
-        const uint64_t Tk = dkey(T);
-        int lo = 0, hi = ns - 1;  // largest r with O_r <= T
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (dkey(O[mid]) <= Tk) lo = mid; else hi = mid - 1;
+    // ---- B. fixed-point chunk totals in the global scale; hot chunks (unordered list)
+    int cnt = 0;
+    for (int c = tid; c < nchn; c += NT) {
+        O[c] = fixp(ctot[c], FIX_F + cexp[c] - Cm);
+        cnt += cmx[c] >= thr ? 1 : 0;
+    }
+    cnt = __reduce_add_sync(FULL, cnt);
+    if (lane == 0 && cnt) atomicAdd(misc + GM_CNT, cnt);
+    __syncthreads();
+    int nhot = misc[GM_CNT];
+    float hthr = thr;
+    if (nhot > HCAP) {
+        // too many qualify: keep the hottest, by a histogram of the maxima over
+        // [thr, M] read from the top until HCAP would be exceeded
+        for (int i = tid; i < HBINS; i += NT) hist[i] = 0;
+        __syncthreads();
+        const float span = fmaxf(M - thr, 1e-30f);
+        for (int c = tid; c < nchn; c += NT) {
+            const float m = cmx[c];
+            if (m >= thr) atomicAdd(hist + min(HBINS - 1, (int)((m - thr) / span * HBINS)), 1);
         }
-        const int r = lo;
-        const double Tl = __dmul_rn(__dsub_rn(T, O[r]), pow2pos(Cm - crs[r]));
-        const uint64_t Tlk = dkey(Tl);
-        const int nck = (min(L, n - r * L) + CHUNK - 1) / CHUNK;
-        const size_t cbase = bhc + (size_t)r * cps;
-        int cst = 0;
-        double cb = 0.0;
-#pragma unroll
-        for (int c = 1; c < CPS_MAX; ++c) {  // coff of chunk 0 is 0
-            if (c < nck) {
-                const double v = __ldcg(p.coff + cbase + c);
-                if (dkey(v) <= Tlk) {
-                    cst = c;
-                    cb = v;
+        __syncthreads();
+        if (tid == 0) {
+            int acc = 0, bin = HBINS;
+            while (bin > 0 && acc + hist[bin - 1] <= HCAP) acc += hist[--bin];
+            misc[GM_CNT] = bin;  // lowest bin kept (HBINS: none fits)
+        }
+        __syncthreads();
+        const int bin = misc[GM_CNT];
+        hthr = bin < HBINS ? thr + span * ((float)bin / HBINS) : __int_as_float(0x7f800000);
+        // (a chunk exactly on a bin edge may land in the bin below: count again)
+        int cc = 0;
+        for (int c = tid; c < nchn; c += NT) cc += cmx[c] >= hthr ? 1 : 0;
+        cc = __reduce_add_sync(FULL, cc);
+        __syncthreads();
+        if (tid == 0) misc[GM_CNT] = 0;
+        __syncthreads();
+        if (lane == 0 && cc) atomicAdd(misc + GM_CNT, cc);
+        __syncthreads();
+        nhot = misc[GM_CNT];
+        if (nhot > HCAP) nhot = 0;  // (ties at the very top: no re-scoring)
+    }
+    if (nhot > 0) {
+        for (int c = tid; c < nchn; c += NT)
+            if (cmx[c] >= hthr) hot[atomicAdd(misc + GM_NHOT, 1)] = c;
+        __syncthreads();
+    }
+
+    // ---- C. heavy keys of the hot chunks: slot q = hot entry * 32 + key
+    float *wrow = p.w + (size_t)bh * p.n_pad;
+    for (int q = tid; q < nhot * CHUNK; q += NT) {
+        const int c = hot[q / CHUNK];
+        const int j = c * CHUNK + (q % CHUNK);
+        if (j < n) {
+            const float wv = __ldcg(wrow + j);
+            if (wv >= exp2f(thr - (float)cexp[c])) {
+                const int pos = atomicAdd(misc + GM_NHV, 1);
+                if (pos < HKCAP) {
+                    hv[pos] = j;
+                    hvw[pos] = wv;
                 }
             }
         }
-        const int shift = __ldcg(p.cshift + cbase + cst);
-        const float rres = (float)__dmul_rn(__dsub_rn(Tl, cb), pow2pos(shift));
-        const int j0 = r * L + cst * CHUNK;
+    }
+    __syncthreads();
+    const int nhv = min(misc[GM_NHV], HKCAP);
+
+    // ---- D. re-score the heavy keys (one thread each) and patch their chunk totals
+    const uint16_t *kg = p.k + ((size_t)b * p.H_kv + g) * (size_t)p.n_max * D;
+    for (int i = tid; i < nhv; i += NT) {
+        const int j = hv[i];
+        const int c = j / CHUNK;
+        const int ct = cexp[c];
+        float shi, slo;
+        rescore_key<D>(kg + (size_t)j * D, qf, p.k2_hi, p.k2_lo, shi, slo);
+        const float wnew = exp2f(__fadd_rn(__fsub_rn(shi, (float)ct), slo));
+        wrow[j] = wnew;
+        const int e = FIX_F + ct - Cm;
+        const uint64_t dx = fixp(wnew, e) - fixp(hvw[i], e);  // two's complement difference
+        if (dx) atomicAdd((unsigned long long *)(O + c), (unsigned long long)dx);
+    }
+    __syncthreads();
+
+    // ---- E. exact exclusive prefix of the G_c: a contiguous range per thread
+    {
+        const int per = (nchn + NT - 1) / NT;
+        const int c0 = min(tid * per, nchn), c1 = min(c0 + per, nchn);
+        uint64_t run = 0;
+        for (int c = c0; c < c1; ++c) run += O[c];
+        // exclusive scan of the per-thread sums over the block
+        uint64_t x = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t y = __shfl_up_sync(FULL, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) scan64[warp] = x;
+        __syncthreads();
+        if (tid == 0) {
+            uint64_t a = 0;
+            for (int w = 0; w < NWARP; ++w) {
+                const uint64_t t = scan64[w];
+                scan64[w] = a;
+                a += t;
+            }
+            scan64[NWARP] = a;
+        }
+        __syncthreads();
+        uint64_t base = scan64[warp] + x - run;
+        for (int c = c0; c < c1; ++c) {
+            const uint64_t v = O[c];
+            O[c] = base;
+            base += v;
+        }
+    }
+    __syncthreads();
+    const uint64_t Z = scan64[NWARP];
+
+    // ---- F. points -> chunk (binary search on O) -> key (the chunk's 32 weights, one line)
+    for (int s = tid; s < S; s += NT) {
+        const uint64_t T = __umul64hi(tfx[s], Z);
+        int lo = 0, hi = nchn - 1;  // largest c with O_c <= T
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (O[mid] <= T) lo = mid; else hi = mid - 1;
+        }
+        const int c = lo;
+        // remainder inside the chunk, in the chunk's own scale 2^-c_t (fp32)
+        const float rres = __fmul_rn(__ull2float_rn(T - O[c]), exp2i(Cm - cexp[c] - FIX_F));
+        const int j0 = c * CHUNK;
         const int jn = min(CHUNK, n - j0);
         const float4 *w4 = reinterpret_cast<const float4 *>(wrow + j0);
         float wv[CHUNK];
@@ -269,63 +335,67 @@ __global__ void __launch_bounds__(NT) santa_gather_kernel(const Params p)
     }
     __syncthreads();
 
-    // ---- sorted indices out; distinct rows (run starts) and their counts
+    // ---- G. sorted indices out; each warp gathers the distinct rows of its run of
+    // points (a row split between two warps is loaded by both, each with its own count)
     if (p.idx_out)
         for (int s = tid; s < S; s += NT) p.idx_out[(size_t)bh * S + s] = idx[s];
-    {
-        const int per = (S + NT - 1) / NT;
-        const int s0 = min(tid * per, S), s1 = min(s0 + per, S);
-        int cnt = 0;
-        for (int s = s0; s < s1; ++s) cnt += (s == 0 || idx[s] != idx[s - 1]) ? 1 : 0;
-        int nlead;
-        int pos = block_excl_scan(cnt, misc, &nlead);
-        for (int s = s0; s < s1; ++s)
-            if (s == 0 || idx[s] != idx[s - 1]) lead[pos++] = s;
-        if (tid == 0) lead[nlead] = S;
-        __syncthreads();
-        // gather-add: warp-strided over the distinct rows, 8 rows in flight per warp
-        float acc[EPL];
+    const uint16_t *vg = p.v + ((size_t)b * p.H_kv + g) * (size_t)p.n_max * D;
+    const int per = (S + NWARP - 1) / NWARP;
+    const int s0 = min(warp * per, S), s1 = min(s0 + per, S);
+    float acc[EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-        const uint16_t *vg = p.v + ((size_t)b * p.H_kv + g) * (size_t)p.n_max * D;
-        constexpr int U = 8;
-        for (int l0 = warp * U; l0 < nlead; l0 += NWARP * U) {
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    for (int base = s0; base < s1; base += 32) {
+        const int s = base + lane;
+        const bool in = s < s1;
+        const int j = in ? idx[s] : 0;
+        // a run starts at each new index and at the first lane of every batch of 32
+        const bool starts = in && (lane == 0 || idx[s - 1] != j);
+        unsigned lead = __ballot_sync(FULL, starts);
+        const unsigned after = lane == 31 ? 0u : (lead & (~0u << (lane + 1)));
+        const int run = (after ? __ffs(after) - 1 : min(32, s1 - base)) - lane;
+        while (lead) {  // (lead is warp-uniform)
+            constexpr int U = 8;
+            int js[U];
+            float cf[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int src = lead ? __ffs(lead) - 1 : 0;
+                const int jv = __shfl_sync(FULL, j, src);
+                const int rn = __shfl_sync(FULL, run, src);
+                js[u] = lead ? jv : 0;
+                cf[u] = lead ? (float)rn : 0.f;
+                lead &= lead - 1u;
+            }
             float vv[U][EPL];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int li = l0 + u;
-                const int j = li < nlead ? idx[lead[li]] : 0;
                 if constexpr (EPL == 4) {
-                    const uint2 raw = *reinterpret_cast<const uint2 *>(vg + (size_t)j * D + 4 * lane);
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(vg + (size_t)js[u] * D + 4 * lane);
                     vv[u][0] = bf16lo_to_f32(raw.x);
                     vv[u][1] = bf16hi_to_f32(raw.x);
                     vv[u][2] = bf16lo_to_f32(raw.y);
                     vv[u][3] = bf16hi_to_f32(raw.y);
                 } else {
-                    const uint32_t raw = *reinterpret_cast<const uint32_t *>(vg + (size_t)j * D + 2 * lane);
+                    const uint32_t raw = *reinterpret_cast<const uint32_t *>(vg + (size_t)js[u] * D + 2 * lane);
                     vv[u][0] = bf16lo_to_f32(raw);
                     vv[u][1] = bf16hi_to_f32(raw);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int li = l0 + u;
-                if (li < nlead) {
-                    const float cf = (float)(lead[li + 1] - lead[li]);
+            for (int u = 0; u < U; ++u)
 #pragma unroll
-                    for (int e = 0; e < EPL; ++e) acc[e] = __fmaf_rn(cf, vv[u][e], acc[e]);
-                }
-            }
+                for (int e = 0; e < EPL; ++e) acc[e] = __fmaf_rn(cf[u], vv[u][e], acc[e]);
         }
+    }
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc_s[warp * D + EPL * lane + e] = acc[e];
-        __syncthreads();
-        for (int i = tid; i < D; i += NT) {
-            float sum = 0.f;
+    for (int e = 0; e < EPL; ++e) acc_s[warp * D + EPL * lane + e] = acc[e];
+    __syncthreads();
+    for (int i = tid; i < D; i += NT) {
+        float sum = 0.f;
 #pragma unroll
-            for (int w = 0; w < NWARP; ++w) sum = __fadd_rn(sum, acc_s[w * D + i]);
-            p.out[(size_t)bh * D + i] = __fdiv_rn(sum, (float)S);
-        }
+        for (int w = 0; w < NWARP; ++w) sum = __fadd_rn(sum, acc_s[w * D + i]);
+        p.out[(size_t)bh * D + i] = __fdiv_rn(sum, (float)S);
     }
 }
 

@@ -6,7 +6,7 @@
 // those V rows, scaled by 1/S.  The score stage is santa_score_kernel
 // (santa_score.cuh), the value stage santa_gather_kernel (santa_gather.cuh); this file
 // holds the pieces they and the dense kernel share: the per-tile grouped-query dot
-// products, the error-free rescoring of heavy keys, the work-item space and small
+// products, the error-free re-scoring of heavy keys, the work-item space and small
 // block-level helpers.
 #pragma once
 
@@ -139,43 +139,47 @@ __device__ __forceinline__ void tile_dots(const uint8_t *tile, int kbase, int su
     rs_step<C::P / 2, 2 * G, 2 * G>(val, sub);
 }
 
-// Error-free dot of one staged K row with query head qf_h (fp32 copies of bf16 values),
-// by the whole warp; returns the score in log2 units as a normalised pair (hi, lo).
+// Error-free score of one K row (global memory) with query head qf (fp32 copies of the
+// bf16 values, shared memory), by one thread.  Products of two bf16 values are exact in
+// fp32; four interleaved compensated sums (Knuth's TwoSum, errors accumulated apart)
+// keep the dependency chains short, and are merged the same way.  Returns the score in
+// log2 units, s * scale * log2(e), as a normalised pair (hi, lo) accurate to about
+// 2^-44 relative.
 template <int D>
-__device__ __forceinline__ void refine_score(const uint8_t *row, const float *qf_h, int lane, float k2_hi,
-                                             float k2_lo, float &hi, float &lo)
+__device__ __forceinline__ void rescore_key(const uint16_t *krow, const float *qf, float k2_hi, float k2_lo,
+                                            float &hi, float &lo)
 {
-    float s, e, t;
-    if constexpr (D == 128) {
-        const uint2 kw = *reinterpret_cast<const uint2 *>(row + 8 * lane);
-        const float4 qv = *reinterpret_cast<const float4 *>(qf_h + 4 * lane);
-        const float p0 = __fmul_rn(qv.x, bf16lo_to_f32(kw.x));
-        const float p1 = __fmul_rn(qv.y, bf16hi_to_f32(kw.x));
-        const float p2 = __fmul_rn(qv.z, bf16lo_to_f32(kw.y));
-        const float p3 = __fmul_rn(qv.w, bf16hi_to_f32(kw.y));
-        two_sum(p0, p1, s, e);
-        two_sum(s, p2, s, t);
-        e = __fadd_rn(e, t);
-        two_sum(s, p3, s, t);
-        e = __fadd_rn(e, t);
-    } else {
-        const uint32_t kw = *reinterpret_cast<const uint32_t *>(row + 4 * lane);
-        const float2 qv = *reinterpret_cast<const float2 *>(qf_h + 2 * lane);
-        two_sum(__fmul_rn(qv.x, bf16lo_to_f32(kw)), __fmul_rn(qv.y, bf16hi_to_f32(kw)), s, e);
-    }
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint4 *k4 = reinterpret_cast<const uint4 *>(krow);
 #pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, m);
-        const float e2 = __shfl_xor_sync(0xffffffffu, e, m);
-        two_sum(s, s2, s, t);
-        e = __fadd_rn(__fadd_rn(e, e2), t);
+    for (int c = 0; c < D / 8; ++c) {  // 16-byte chunks of 8 elements
+        const uint4 kv = __ldcg(k4 + c);
+        const uint32_t wv[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int d0 = 8 * c + 2 * i;
+            const int a = (2 * i) & 3, b2 = (2 * i + 1) & 3;
+            float t;
+            two_sum(s[a], __fmul_rn(qf[d0], bf16lo_to_f32(wv[i])), s[a], t);
+            e[a] = __fadd_rn(e[a], t);
+            two_sum(s[b2], __fmul_rn(qf[d0 + 1], bf16hi_to_f32(wv[i])), s[b2], t);
+            e[b2] = __fadd_rn(e[b2], t);
+        }
     }
-    fast_two_sum(s, e, s, e);
-    // (s + e) * (k2_hi + k2_lo) to about 2^-46 relative
-    const float P = __fmul_rn(s, k2_hi);
-    float E = __fmaf_rn(s, k2_hi, -P);
-    E = __fmaf_rn(s, k2_lo, E);
-    E = __fmaf_rn(e, k2_hi, E);
+    float S0, E0, S1, E1, t;
+    two_sum(s[0], s[1], S0, t);
+    E0 = __fadd_rn(__fadd_rn(e[0], e[1]), t);
+    two_sum(s[2], s[3], S1, t);
+    E1 = __fadd_rn(__fadd_rn(e[2], e[3]), t);
+    float sum, err;
+    two_sum(S0, S1, sum, t);
+    err = __fadd_rn(__fadd_rn(E0, E1), t);
+    fast_two_sum(sum, err, sum, err);
+    // (sum + err) * (k2_hi + k2_lo) to about 2^-46 relative
+    const float P = __fmul_rn(sum, k2_hi);
+    float E = __fmaf_rn(sum, k2_hi, -P);
+    E = __fmaf_rn(sum, k2_lo, E);
+    E = __fmaf_rn(err, k2_hi, E);
     fast_two_sum(P, E, hi, lo);
 }
 

@@ -1,53 +1,59 @@
-// santa_score.cuh -- SANTA score stage: scores, weights and the CDF pieces, sm_103a.
+// santa_score.cuh -- SANTA score stage: scores, weights and per-chunk CDF pieces, sm_103a.
 //
 // "Stochastic Sparse Attention for Memory-Bound Inference" (abstract): the score stage
 // reads all n_k cached keys and forms the post-softmax distribution from which the
 // value stage samples.  This is the kernel that streams the K cache (about 97% of the
 // bytes of a sampled decode step), so it is built for bandwidth:
 //
-//  * persistent CTAs of 8 independent warps; a warp takes a whole split (b, g, r) --
-//    L consecutive keys of KV head g of batch row b -- from a global work counter and
-//    streams it through its own ring of 32-key tiles, filled by 1-D TMA bulk copies
-//    (cp.async.bulk, completion on an mbarrier) that lane 0 issues;
+//  * persistent CTAs of 8 independent warps; a warp takes work units of L consecutive
+//    keys of one KV head g of one batch row b from a global counter -- two units per
+//    grab while much work remains, one at a time near the end, so that the warps finish
+//    together; each grab is requested one grab ahead -- and streams them through its own ring of 32-key tiles, filled by 1-D
+//    TMA bulk copies (cp.async.bulk, completion on an mbarrier) that lane 0 issues;
+//  * the group's query heads ride along with the first tile of a new (b, g) as a second
+//    bulk copy on the same barrier, so a warp does not stall on a query load;
 //  * no CTA-wide barrier after the prologue: a warp waits only for its own tiles;
-//  * one 32-key tile is one CDF chunk, so every per-chunk quantity is a warp-local
-//    reduction over the lanes that hold the same query head.
+//  * one tile is one CDF chunk of 32 keys with its own power-of-two scale, so chunks
+//    are independent: nothing is carried from one tile to the next.
 //
-// Per query head of the group it leaves in the workspace:
-//   w_j      fp32 weight 2^(s_j log2 e - c_t), c_t = ceil of the split's running maximum
-//            (in log2 units) at the key's chunk, so w_j <= 1
-//   cmax     the chunk's maximum of s_j log2 e (fp32)
-//   coff     fp64 exclusive prefix of the chunk totals within the split, in the split's
-//            scale 2^-c_r, and cshift = c_r - c_t of each chunk
-//   split_W  fp64 split total, split_c = c_r, split_m = the split's maximum score
-// Rescaling between chunk and split scales is by powers of two (exact in fp64).
+// Per query head of the group and per chunk it leaves in the workspace:
+//   w_j    fp32 weight 2^(s_j log2 e - c_t), c_t = ceil(the chunk's maximum of s log2 e),
+//          so every w_j <= 1 and the chunk's heaviest key has w > 1/2
+//   ctot   the chunk total of the w_j (fp32, summed over the warp in a fixed tree)
+//   cexp   c_t (int32)
+//   cmax   the chunk's maximum of s log2 e (fp32)
+// The value stage turns these into one exact fixed-point prefix per head.
 //
 // Weights are computed with one rounding of the small exponent s log2e - c_t (two
 // fused multiply-adds with scale*log2e split into an fp32 pair), so the keys at the
 // top of the distribution carry only the dot product's own rounding.  The value stage
-// later re-scores error-free the few keys within tau2 of the global maximum (found
-// from cmax), where that rounding would move later CDF boundaries most.
+// re-scores error-free the few keys within tau2 of the global maximum (found from
+// cmax), where that rounding would move later CDF boundaries most.
 #pragma once
 
 #include "santa_sample.cuh"
 
 namespace santa {
 
-template <int D>
+template <int D, int G>
 struct ScoreTile {
-    static constexpr int KEYS = CHUNK;                 // keys per warp tile = one CDF chunk
-    static constexpr int BYTES = KEYS * 2 * D;         // 8 KB at d=128, 4 KB at d=64
-    static constexpr int NSTAGE = 24576 / BYTES;       // 24 KB of ring per warp
+    static constexpr int KEYS = CHUNK;                   // keys per warp tile = one CDF chunk
+    static constexpr int BYTES = KEYS * 2 * D;           // 8 KB at d=128, 4 KB at d=64
+    static constexpr int NSTAGE = 24576 / BYTES;         // 24 KB of ring per warp
+    static constexpr int QBYTES = G * D * 2;             // the group's query heads, bf16
+    static constexpr int QBUF = QBYTES <= 1024 ? 2 : 1;  // staging buffers for them
 };
 
 struct ScoreSmem {
-    int nb, prefix, misc, warp0, warp_bytes, ring, bar, desc, ctot, cexp, total;
+    int nb, prefix, misc, warp0, warp_bytes, ring, qbuf, bar, desc, total;
 };
 
 __host__ __device__ inline ScoreSmem score_smem(int D, int G, int B)
 {
     const int bytes = CHUNK * 2 * D;
     const int nstage = 24576 / bytes;
+    const int qbytes = G * D * 2;
+    const int qbuf = qbytes <= 1024 ? 2 : 1;
     ScoreSmem s{};
     int off = 0;
     s.nb = off; off += (int)align_up((size_t)B * 4, 16);
@@ -57,20 +63,23 @@ __host__ __device__ inline ScoreSmem score_smem(int D, int G, int B)
     // per-warp block (offsets relative to the warp's base)
     int w = 0;
     s.ring = w; w += nstage * bytes;
+    s.qbuf = w; w += qbuf * qbytes;
     s.bar = w; w += nstage * 8;
     s.desc = w = (int)align_up((size_t)w, 16); w += nstage * 16;
-    s.ctot = w; w += G * CPS_MAX * 4;
-    s.cexp = w; w += G * CPS_MAX * 4;
     s.warp_bytes = (int)align_up((size_t)w, 128);
     s.total = s.warp0 + NWARP * s.warp_bytes;
     return s;
 }
 
+// Tile descriptor flags (int4.w): the tile is the first of a new (b, g); its query heads
+// come in staging buffer (flags >> TF_QB_SHIFT) & 1, or are read from global memory.
+enum : int { TF_NEWQ = 1, TF_QGLOBAL = 2, TF_QB_SHIFT = 2 };
+
 template <int D, int G>
 __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
 {
     using C = SampleCfg<D, G>;
-    using T = ScoreTile<D>;
+    using T = ScoreTile<D, G>;
     constexpr int NSTAGE = T::NSTAGE;
     constexpr int NCALL = T::KEYS / C::KW;  // tile_dots calls per tile
     constexpr int NV = C::NV;
@@ -78,17 +87,16 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sub = lane % C::P, grp = lane / C::P;
-    const int B = p.B, H_kv = p.H_kv, H_q = p.H_q, L = p.L;
+    const int B = p.B, H_kv = p.H_kv, H_q = p.H_q, L = p.L;  // L: keys per work unit
     const ScoreSmem lay = score_smem(D, G, B);
     int *nb = reinterpret_cast<int *>(smem + lay.nb);
     int *prefix = reinterpret_cast<int *>(smem + lay.prefix);
     int *misc = reinterpret_cast<int *>(smem + lay.misc);
     uint8_t *wb = smem + lay.warp0 + warp * lay.warp_bytes;
     uint8_t *ring = wb + lay.ring;
+    uint8_t *qbuf = wb + lay.qbuf;
     uint64_t *bars = reinterpret_cast<uint64_t *>(wb + lay.bar);
     int4 *desc = reinterpret_cast<int4 *>(wb + lay.desc);
-    float *ctot = reinterpret_cast<float *>(wb + lay.ctot);  // [G][CPS_MAX]
-    int *cexp = reinterpret_cast<int *>(wb + lay.cexp);      // [G][CPS_MAX]
     const float NEG_INF = __int_as_float(0xff800000);
 
     build_item_space(p, nb, prefix, misc);
@@ -98,52 +106,92 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
     }
     __syncthreads();  // the only CTA-wide barrier of the main path
     const int total_items = prefix[B];
+    // grab two units at a time until the last two rounds' worth of single units
+    const int tail_from = total_items - 2 * (int)gridDim.x * NWARP;
 
-    // ---- producer state (warp-uniform; lane 0 issues the copies and the atomics)
+    // ---- producer state (warp-uniform; lane 0 issues the copies and the atomics).  The
+    // next grab is requested one grab ahead, so its atomic never stalls the warp.
     uint64_t policy = 0;
-    int pend = 0;  // lane 0: the next item index, fetched one item ahead
-    if (lane == 0) {
-        policy = l2_policy_evict_first();
-        pend = atomicAdd(p.ctrl + CTRL_WORK, 1);
-    }
-    int pr_item = 0, pr_tile = 0, pr_ntiles = 0, pr_valid = 0;
+    int pend = 0;               // lane 0: the answer of the outstanding grab (index*8 + size)
+    auto request = [&](int last) {
+        if (lane == 0) {
+            const int k = (last < tail_from) ? 2 : 1;  // two units while far from the end
+            pend = atomicAdd(p.ctrl + CTRL_WORK, k) * 8 + k;
+        }
+    };
+    if (lane == 0) policy = l2_policy_evict_first();
+    request(0);
+    int g_next = 0, g_end = 0;  // the current grab [g_next, g_end)
+    int pr_item = 0, pr_tile = 0, pr_ntiles = 0, pr_valid = 0, pr_grp = 0;
     long long pr_row0 = 0;
     bool pr_end = false;
-    auto produce = [&](int slot) {
+    int pr_group = -1;          // (b * H_kv + g) of the last unit issued
+    int q_issue0 = -1, q_issue1 = -1;  // sequence number of the tile carrying each q buffer
+    int q_next = 0;             // the q buffer to use next
+    int pr_seq = 0;             // sequence number of the next tile issued
+    auto produce = [&](int slot, int cons_seq) {
         while (!pr_end && pr_tile == pr_ntiles) {
-            const int it = __shfl_sync(FULL, pend, 0);
-            if (it >= total_items) {
-                pr_end = true;
-                break;
+            if (g_next == g_end) {
+                const int got = __shfl_sync(FULL, pend, 0);
+                g_next = got >> 3;
+                g_end = min(g_next + (got & 7), total_items);
+                if (g_next >= total_items) {
+                    pr_end = true;
+                    break;
+                }
+                request(g_end);
             }
-            if (lane == 0) pend = atomicAdd(p.ctrl + CTRL_WORK, 1);
-            const Item x = decode_item(it, prefix, nb, B, H_kv, L);
+            const int itm = g_next++;
+            const Item x = decode_item(itm, prefix, nb, B, H_kv, L);
             if (x.n == 0) continue;  // empty rows are written by the value stage
-            pr_item = it;
+            pr_item = itm;
             pr_tile = 0;
             pr_valid = min(L, x.n - x.r * L);
             pr_ntiles = (pr_valid + T::KEYS - 1) / T::KEYS;
             pr_row0 = ((long long)x.b * H_kv + x.g) * p.n_max + (long long)x.r * L;
+            pr_grp = x.b * H_kv + x.g;
         }
         if (pr_end) {
             if (lane == 0) desc[slot] = make_int4(DESC_END, 0, 0, 0);
             return;
         }
         const int rows = min(T::KEYS, pr_valid - pr_tile * T::KEYS);
+        int flags = 0;
+        uint32_t qbytes = 0;
+        int qb = 0;
+        if (pr_tile == 0) {
+            if (pr_grp != pr_group) {
+                pr_group = pr_grp;
+                flags |= TF_NEWQ;
+                qb = (T::QBUF == 2) ? q_next : 0;
+                const int busy = qb ? q_issue1 : q_issue0;
+                // a staging buffer is free once the consumer has started the tile that carried it
+                if (busy <= cons_seq) {
+                    if (qb) q_issue1 = pr_seq; else q_issue0 = pr_seq;
+                    if (T::QBUF == 2) q_next ^= 1;
+                    flags |= qb << TF_QB_SHIFT;
+                    qbytes = T::QBYTES;
+                } else {
+                    flags |= TF_QGLOBAL;
+                }
+            }
+        }
         if (lane == 0) {
-            desc[slot] = make_int4(pr_item, pr_tile, rows, pr_tile == pr_ntiles - 1 ? FLAG_LAST : 0);
+            desc[slot] = make_int4(pr_item, pr_tile, rows, flags);
             const uint32_t bytes = (uint32_t)rows * C::ROWB;
-            mbar_arrive_tx(&bars[slot], bytes);
+            mbar_arrive_tx(&bars[slot], bytes + qbytes);
             bulk_g2s(ring + slot * T::BYTES, p.k + (pr_row0 + (long long)pr_tile * T::KEYS) * D, bytes,
                      &bars[slot], policy);
+            // q[b][g*G .. g*G+G-1][:] is contiguous: the group's heads in one copy
+            if (qbytes) bulk_g2s_plain(qbuf + qb * T::QBYTES, p.q + (size_t)pr_grp * G * D, qbytes, &bars[slot]);
         }
         ++pr_tile;
+        ++pr_seq;
     };
-    for (int s = 0; s < NSTAGE; ++s) produce(s);
+    for (int s = 0; s < NSTAGE; ++s) produce(s, -1);
 
-    // ---- consumer state (warp-uniform except for the per-lane head slots)
+    // ---- consumer
     unsigned long long qp[G][8];
-    float runmax[NV];
     Item cur{0, 0, 0, 0, 1};
     bool aborted = false;
     int it = 0;
@@ -156,22 +204,21 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
             aborted = true;
             break;
         }
-        const int tile = dsc.y, rows = dsc.z;
-        if (tile == 0) {
-            // a new split: its group's query heads into registers (fp32 pairs of the
-            // lane's two 16-byte chunks of each head)
-            cur = decode_item(dsc.x, prefix, nb, B, H_kv, L);
-            const uint16_t *qg = p.q + ((size_t)cur.b * H_q + (size_t)cur.g * G) * D;
+        const int tile = dsc.y, rows = dsc.z, flags = dsc.w;
+        if (tile == 0) cur = decode_item(dsc.x, prefix, nb, B, H_kv, L);
+        if (flags & TF_NEWQ) {
+            // the group's query heads: fp32 pairs of the lane's two 16-byte chunks per head
+            const uint16_t *qg = (flags & TF_QGLOBAL)
+                                     ? p.q + ((size_t)cur.b * H_q + (size_t)cur.g * G) * D
+                                     : reinterpret_cast<const uint16_t *>(qbuf + ((flags >> TF_QB_SHIFT) & 1) * T::QBYTES);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const uint4 a = __ldg(reinterpret_cast<const uint4 *>(qg + h * D + 8 * sub));
-                const uint4 c = __ldg(reinterpret_cast<const uint4 *>(qg + h * D + 8 * (sub + C::P)));
+                const uint4 a = *reinterpret_cast<const uint4 *>(qg + h * D + 8 * sub);
+                const uint4 c = *reinterpret_cast<const uint4 *>(qg + h * D + 8 * (sub + C::P));
                 const uint32_t wv[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) qp[h][i] = bf16x2_to_f32x2(wv[i]);
             }
-#pragma unroll
-            for (int i = 0; i < NV; ++i) runmax[i] = NEG_INF;
         }
 
         // ---- dot products: call c covers keys [c*KW, c*KW + KW) of the tile
@@ -185,9 +232,9 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
             for (int i = 0; i < NV; ++i) sc[c][i] = val[i];
         }
         __syncwarp();
-        produce(slot);  // the tile's data is in registers: refill its slot now
+        produce(slot, it);  // the tile and the query heads are in registers: refill the slot
 
-        // ---- chunk maximum (log2 units), running maximum and the chunk's scale c_t
+        // ---- the chunk's maximum (log2 units) and its scale c_t
         const bool own = (sub % C::REP) == 0;
         float tmx[NV], ct[NV];
 #pragma unroll
@@ -202,18 +249,17 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
             for (int msk = 1; msk < 32; msk <<= 1)
                 if (C::SAME & (unsigned)msk) m = fmaxf(m, __shfl_xor_sync(FULL, m, msk));
             tmx[i] = m;
-            runmax[i] = fmaxf(runmax[i], m);
-            ct[i] = ceilf(fminf(fmaxf(runmax[i], -16777216.f), 16777216.f));
+            ct[i] = ceilf(fminf(fmaxf(m, -16777216.f), 16777216.f));
         }
 
-        // ---- weights (stored), chunk totals
+        // ---- weights (stored) and the chunk totals
         const size_t bh0 = (size_t)cur.b * H_q + (size_t)cur.g * G;
-        const size_t jbase = (size_t)cur.r * L + (size_t)tile * T::KEYS;
+        const size_t chunk = (size_t)cur.r * (L / CHUNK) + (size_t)tile;  // chunk index in the sequence
         float tot[NV];
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int h = C::head_of(lane, i);
-            float* wrow = p.w + (bh0 + h) * p.n_pad + jbase;
+            float *wrow = p.w + (bh0 + h) * p.n_pad + chunk * CHUNK;
             float acc = 0.f;
 #pragma unroll
             for (int c = 0; c < NCALL; ++c) {
@@ -233,55 +279,13 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
             tot[i] = acc;
         }
         // one lane per head records the chunk (lane bits outside SAME select the head)
-        const int cidx = tile;  // chunk index within the split
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             if ((lane & C::SAME) == 0 && own) {
-                const int h = C::head_of(lane, i);
-                ctot[h * CPS_MAX + cidx] = tot[i];
-                cexp[h * CPS_MAX + cidx] = (int)ct[i];
-                p.cmax[(bh0 + h) * p.nch + (size_t)cur.r * (L / CHUNK) + cidx] = tmx[i];
-                if (dsc.w & FLAG_LAST) p.split_m[(bh0 + h) * p.ns_max + cur.r] = runmax[i];
-            }
-        }
-
-        // ---- split end: chunk prefix within the split, split total and scales.  Lanes
-        // form 32/CPS_MAX segments of CPS_MAX lanes, one head per segment and pass.
-        if (dsc.w & FLAG_LAST) {
-            __syncwarp();
-            const int nchunks = tile + 1;
-            constexpr int SEG = CPS_MAX, HPP = 32 / SEG;
-            const int c = lane % SEG;
-#pragma unroll
-            for (int h0 = 0; h0 < G; h0 += HPP) {
-                const int h = h0 + lane / SEG;
-                const bool act = h < G && c < nchunks;
-                float x32 = 0.f;
-                int ce = INT_MIN;
-                if (act) {
-                    x32 = ctot[h * CPS_MAX + c];
-                    ce = cexp[h * CPS_MAX + c];
-                }
-                int cr = ce;
-#pragma unroll
-                for (int msk = SEG / 2; msk >= 1; msk >>= 1) cr = max(cr, __shfl_xor_sync(FULL, cr, msk));
-                const double x = act ? __dmul_rn((double)x32, pow2d(ce - cr)) : 0.0;
-                double incl = x;
-#pragma unroll
-                for (int o = 1; o < SEG; o <<= 1) {
-                    const double y = __shfl_up_sync(FULL, incl, o);
-                    if (c >= o) incl = __dadd_rn(incl, y);
-                }
-                const size_t bh = bh0 + (size_t)(h < G ? h : 0);
-                if (act) {
-                    const size_t ci = bh * p.nch + (size_t)cur.r * (L / CHUNK) + c;
-                    p.coff[ci] = __dsub_rn(incl, x);
-                    p.cshift[ci] = cr - ce;
-                }
-                if (h < G && c == SEG - 1) {
-                    p.split_W[bh * p.ns_max + cur.r] = incl;
-                    p.split_c[bh * p.ns_max + cur.r] = cr;
-                }
+                const size_t ci = (bh0 + C::head_of(lane, i)) * p.nch + chunk;
+                p.ctot[ci] = tot[i];
+                p.cexp[ci] = (int)ct[i];
+                p.cmax[ci] = tmx[i];
             }
         }
     }

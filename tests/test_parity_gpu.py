@@ -57,6 +57,8 @@ CASES = [
     (64, 8, 4, 2500, [2500, 2048], 128),
     (64, 16, 4, 900, [900, 64, 129], 256),
     (64, 64, 8, 700, [700, 311], 48),
+    # more than 4096 chunks: the value stage keeps its chunk arrays in global memory
+    (64, 8, 2, 140000, [140000, 3000], 200),
 ]
 
 
@@ -83,6 +85,23 @@ def test_small_parity(d, H_q, H_kv, n_max, seq, S, mode):
     same = [(b, h) for b in nz for h in range(H_q) if np.array_equal(idx[b, h], i_ref[b, h])]
     sel = tuple(np.array(same).T)
     assert np.abs(o[sel] - o_ref[sel]).max() <= 1e-2
+
+
+@pytest.mark.parametrize("score_std", [0.0, 0.05, 0.5, 1.0, 6.0])
+@pytest.mark.parametrize("mode", ["systematic", "stratified"])
+def test_flat_and_peaked_scores(score_std, mode):
+    """Score spreads from exactly flat (q = 0: every weight is 1, so the CDF is exact on
+    both sides) through near-flat (every chunk lies near the maximum, so the set of
+    chunks that get heavy-key re-scoring is capped) to very peaked (std 6)."""
+    seq = [6000, 4097]
+    w, q, k, v, sl = workloads.small("spread", 2, 8, 2, 128, 6000, 512, seq_lens=seq,
+                                     score_std=score_std, seed=int(score_std * 100) + 3)
+    out, idx = run(q, k, v, sl, 512, mode, seed=5)
+    o_ref, i_ref = oracle.decode(q, k, v, sl, 512, mode, seed=5)
+    if score_std == 0.0:
+        assert np.array_equal(idx, i_ref)
+    check_indices(idx, i_ref, q, k, sl, 512, mode, 5)
+    check_estimator(out.numpy(), idx, v, sl, o_ref)
 
 
 @pytest.mark.parametrize("d,H_q,H_kv,n_max,seq,S", CASES)
