@@ -154,6 +154,23 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
     return p;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Global stores with an L2 cache policy (data the next kernel reads back).
+__device__ __forceinline__ void st_hint(float *a, float v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(a), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_hint(int *a, int v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.s32 [%0], %1, %2;" ::"l"(a), "r"(v), "l"(pol) : "memory");
+}
+
 // 1-D bulk copy global -> shared (TMA engine), completion counted on `bar` in bytes.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,

@@ -6,10 +6,11 @@
 // bytes of a sampled decode step), so it is built for bandwidth:
 //
 //  * persistent CTAs of 8 independent warps; a warp takes work units of L consecutive
-//    keys of one KV head g of one batch row b from a global counter -- two units per
-//    grab while much work remains, one at a time near the end, so that the warps finish
-//    together; each grab is requested one grab ahead -- and streams them through its own ring of 32-key tiles, filled by 1-D
-//    TMA bulk copies (cp.async.bulk, completion on an mbarrier) that lane 0 issues;
+//    keys of one KV head g of one batch row b -- a static contiguous block of units
+//    first, then grabs from a global counter that shrink to single units near the end,
+//    so that the warps finish together -- and streams them through its own ring of 32-key tiles, filled by 1-D TMA bulk copies (cp.async.bulk, completion
+//    on an mbarrier) that lane 0 issues; K is read with an L2 evict-first hint, and the
+//    weights and chunk data are written with evict-last, for the value stage;
 //  * the group's query heads ride along with the first tile of a new (b, g) as a second
 //    bulk copy on the same barrier, so a warp does not stall on a query load;
 //  * no CTA-wide barrier after the prologue: a warp waits only for its own tiles;
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sub = lane % C::P, grp = lane / C::P;
-    const int B = p.B, H_kv = p.H_kv, H_q = p.H_q, L = p.L;  // L: keys per work unit
+    const int B = p.B, H_kv = p.H_kv, L = p.L;  // L: keys per work unit
     const ScoreSmem lay = score_smem(D, G, B);
     int *nb = reinterpret_cast<int *>(smem + lay.nb);
     int *prefix = reinterpret_cast<int *>(smem + lay.prefix);
@@ -106,29 +107,55 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
     }
     __syncthreads();  // the only CTA-wide barrier of the main path
     const int total_items = prefix[B];
-    // grab two units at a time until the last two rounds' worth of single units
-    const int tail_from = total_items - 2 * (int)gridDim.x * NWARP;
+    // Work schedule: about 80% of the units as one contiguous static block per warp (no
+    // atomics, long sequential streams); the rest handed out from a global counter in
+    // grabs that shrink from four units to one as the work runs out, so that the warps
+    // finish together.  Each grab is requested one grab ahead, so its atomic never
+    // stalls the warp.
+    const int W = (int)gridDim.x * NWARP;
+    const int gw = (int)blockIdx.x * NWARP + warp;
+    const int Ks = (int)((long long)total_items * 4 / 5 / W);  // static units per warp
+    const int dyn0 = Ks * W;                                    // the first dynamic unit
 
-    // ---- producer state (warp-uniform; lane 0 issues the copies and the atomics).  The
-    // next grab is requested one grab ahead, so its atomic never stalls the warp.
+    // ---- producer state (warp-uniform; lane 0 issues the copies and the atomics)
     uint64_t policy = 0;
-    int pend = 0;               // lane 0: the answer of the outstanding grab (index*8 + size)
+    const uint64_t keep = l2_policy_evict_last();  // the value stage reads these back
+    int pend = 0;  // lane 0: the outstanding grab, first unit * 8 + size
     auto request = [&](int last) {
         if (lane == 0) {
-            const int k = (last < tail_from) ? 2 : 1;  // two units while far from the end
-            pend = atomicAdd(p.ctrl + CTRL_WORK, k) * 8 + k;
+            const int k = max(1, min(4, (total_items - last) / (2 * W)));
+            pend = (dyn0 + atomicAdd(p.ctrl + CTRL_WORK, k)) * 8 + k;
         }
     };
     if (lane == 0) policy = l2_policy_evict_first();
-    request(0);
-    int g_next = 0, g_end = 0;  // the current grab [g_next, g_end)
-    int pr_item = 0, pr_tile = 0, pr_ntiles = 0, pr_valid = 0, pr_grp = 0;
+    request(dyn0);
+    int g_next = gw * Ks, g_end = g_next + Ks;  // the current grab: the static block first
+    int pr_r = 0, pr_tile = 0, pr_ntiles = 0, pr_valid = 0, pr_grp = 0;
     long long pr_row0 = 0;
     bool pr_end = false;
     int pr_group = -1;          // (b * H_kv + g) of the last unit issued
     int q_issue0 = -1, q_issue1 = -1;  // sequence number of the tile carrying each q buffer
     int q_next = 0;             // the q buffer to use next
     int pr_seq = 0;             // sequence number of the next tile issued
+    // position (b, g, r) of unit g_next, found by one search per grab and then stepped
+    int ub = 0, ug = 0, ur = 0, uns = 1;
+    auto seek = [&](int itm) {
+        const Item x = decode_item(itm, prefix, nb, B, H_kv, L);
+        ub = x.b;
+        ug = x.g;
+        ur = x.r;
+        uns = x.ns;
+    };
+    auto step = [&]() {
+        if (++ur == uns) {
+            ur = 0;
+            if (++ug == H_kv) {
+                ug = 0;
+                if (++ub < B) uns = nb[ub] > 0 ? (nb[ub] + L - 1) / L : 1;
+            }
+        }
+    };
+    if (g_next < g_end) seek(g_next);
     auto produce = [&](int slot, int cons_seq) {
         while (!pr_end && pr_tile == pr_ntiles) {
             if (g_next == g_end) {
@@ -140,16 +167,19 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
                     break;
                 }
                 request(g_end);
+                seek(g_next);
             }
-            const int itm = g_next++;
-            const Item x = decode_item(itm, prefix, nb, B, H_kv, L);
-            if (x.n == 0) continue;  // empty rows are written by the value stage
-            pr_item = itm;
+            const int n = nb[ub];
+            const int b = ub, g = ug, r = ur;
+            ++g_next;
+            step();
+            if (n == 0) continue;  // empty rows are written by the value stage
+            pr_r = r;
             pr_tile = 0;
-            pr_valid = min(L, x.n - x.r * L);
+            pr_valid = min(L, n - r * L);
             pr_ntiles = (pr_valid + T::KEYS - 1) / T::KEYS;
-            pr_row0 = ((long long)x.b * H_kv + x.g) * p.n_max + (long long)x.r * L;
-            pr_grp = x.b * H_kv + x.g;
+            pr_grp = b * H_kv + g;
+            pr_row0 = (long long)pr_grp * p.n_max + (long long)r * L;
         }
         if (pr_end) {
             if (lane == 0) desc[slot] = make_int4(DESC_END, 0, 0, 0);
@@ -177,7 +207,7 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
             }
         }
         if (lane == 0) {
-            desc[slot] = make_int4(pr_item, pr_tile, rows, flags);
+            desc[slot] = make_int4(pr_grp, (pr_r << 8) | pr_tile, rows, flags);
             const uint32_t bytes = (uint32_t)rows * C::ROWB;
             mbar_arrive_tx(&bars[slot], bytes + qbytes);
             bulk_g2s(ring + slot * T::BYTES, p.k + (pr_row0 + (long long)pr_tile * T::KEYS) * D, bytes,
@@ -192,7 +222,6 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
 
     // ---- consumer
     unsigned long long qp[G][8];
-    Item cur{0, 0, 0, 0, 1};
     bool aborted = false;
     int it = 0;
     for (;; ++it) {
@@ -204,12 +233,12 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
             aborted = true;
             break;
         }
-        const int tile = dsc.y, rows = dsc.z, flags = dsc.w;
-        if (tile == 0) cur = decode_item(dsc.x, prefix, nb, B, H_kv, L);
+        // descriptor: group b*H_kv + g, (unit r << 8) | tile, rows, flags
+        const int grpid = dsc.x, tile = dsc.y & 0xff, ur_c = dsc.y >> 8, rows = dsc.z, flags = dsc.w;
         if (flags & TF_NEWQ) {
             // the group's query heads: fp32 pairs of the lane's two 16-byte chunks per head
             const uint16_t *qg = (flags & TF_QGLOBAL)
-                                     ? p.q + ((size_t)cur.b * H_q + (size_t)cur.g * G) * D
+                                     ? p.q + (size_t)grpid * G * D
                                      : reinterpret_cast<const uint16_t *>(qbuf + ((flags >> TF_QB_SHIFT) & 1) * T::QBYTES);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
@@ -253,8 +282,8 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
         }
 
         // ---- weights (stored) and the chunk totals
-        const size_t bh0 = (size_t)cur.b * H_q + (size_t)cur.g * G;
-        const size_t chunk = (size_t)cur.r * (L / CHUNK) + (size_t)tile;  // chunk index in the sequence
+        const size_t bh0 = (size_t)grpid * G;  // first query head of the group: b*H_q + g*G
+        const size_t chunk = (size_t)ur_c * (L / CHUNK) + (size_t)tile;  // chunk index in the sequence
         float tot[NV];
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
@@ -268,7 +297,7 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
                     const float e = __fmaf_rn(sc[c][i], p.k2_lo, __fmaf_rn(sc[c][i], p.k2_hi, -ct[i]));
                     const float w = exp2f(e);
                     if (own) {
-                        wrow[key] = w;
+                        st_hint(wrow + key, w, keep);
                         acc = __fadd_rn(acc, w);
                     }
                 }
@@ -283,9 +312,9 @@ __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
         for (int i = 0; i < NV; ++i) {
             if ((lane & C::SAME) == 0 && own) {
                 const size_t ci = (bh0 + C::head_of(lane, i)) * p.nch + chunk;
-                p.ctot[ci] = tot[i];
-                p.cexp[ci] = (int)ct[i];
-                p.cmax[ci] = tmx[i];
+                st_hint(p.ctot + ci, tot[i], keep);
+                st_hint(p.cexp + ci, (int)ct[i], keep);
+                st_hint(p.cmax + ci, tmx[i], keep);
             }
         }
     }
