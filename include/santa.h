@@ -39,6 +39,8 @@ extern "C" {
 #define SANTA_ERR_UNSUPPORTED (-4)  /* valid but outside the compiled limits (d, G, S, B) */
 #define SANTA_ERR_CUDA (-5)         /* a CUDA launch or runtime call failed */
 #define SANTA_ERR_DEVICE (-6)       /* the device reported an error (santa_device_status) */
+#define SANTA_ERR_SCRATCH (-7)      /* santa_decode_static: the problem needs more scratch than
+                                       SANTA_STATIC_SCRATCH_BYTES */
 
 /* Value-stage modes ("stratified and systematic sampling", abstract; iid is plain
  * multinomial sampling, the estimator before variance reduction). */
@@ -119,6 +121,38 @@ int santa_sample_points(int32_t B, int32_t H_q, int32_t S, int32_t mode, uint64_
  * Returns SANTA_OK, or SANTA_ERR_DEVICE when *code != 0.
  */
 int santa_device_status(void *workspace, int32_t *code, void *stream);
+
+/*
+ * santa_decode_static -- santa_decode without a caller-provided workspace.  (The pages
+ * have no counterpart: this is an interface convenience of this library.)
+ *
+ * For callers that cannot allocate device memory themselves: code that runs where the
+ * device allocator belongs to someone else (a serving runtime with its own fixed pool,
+ * a plugin that may not call cudaMalloc), or on a path where an allocation would stall
+ * or is not allowed.  The library keeps one scratch buffer of SANTA_STATIC_SCRATCH_BYTES
+ * in a file-scope device array instead; every GPU that loads the library holds that
+ * buffer until the process exits.  This call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ * Arguments and results are those of santa_decode, minus the workspace.  The caller
+ * still passes q, the caches, seq_lens, out and idx_out.
+ *
+ *  - Size limit: the call returns SANTA_ERR_SCRATCH, before touching the device, when
+ *    santa_workspace_size(shape, S, mode) exceeds SANTA_STATIC_SCRATCH_BYTES (for
+ *    example B=1, H_q=32, d=128 fits up to about 110k keys).
+ *  - First call per device: it looks up the device address of the scratch array
+ *    (cudaGetSymbolAddress, with that device current), which can load the library's
+ *    device code.  Make that first call before any stream capture.
+ *  - Every call on a device shares the one buffer.  Each call clears the buffer's
+ *    control block (an asynchronous memset on `stream`) and overwrites the rest, so
+ *    contents left by an earlier call do no harm.  Calls that can overlap on the GPU
+ *    (different streams without ordering, or several host threads) race on the buffer:
+ *    order them on one stream.
+ */
+#define SANTA_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+int santa_decode_static(const santa_shape *shape, const void *q, const void *k_cache,
+                        const void *v_cache, const int32_t *seq_lens, int32_t S, int32_t mode,
+                        uint64_t seed, float *out, int32_t *idx_out, void *stream);
 
 /* santa_status_string -- static description of a status code. */
 const char *santa_status_string(int status);

@@ -83,6 +83,9 @@ const void *points_iid_kernel() { return (const void *)santa_points_iid_kernel; 
 
 // ---------------------------------------------------------------- per-device caches
 
+constexpr int MAX_DEV_STATIC = 64;
+std::mutex g_static_mu;
+
 namespace {
 
 constexpr int MAX_DEV = 64;
@@ -207,6 +210,7 @@ const char *santa_status_string(int status)
                                       "n_max <= 524288, S <= 4096, shared memory)";
     case SANTA_ERR_CUDA: return "CUDA runtime error";
     case SANTA_ERR_DEVICE: return "device reported an error (bad seq_lens or a barrier timeout)";
+    case SANTA_ERR_SCRATCH: return "the problem needs more scratch than the static buffer of santa_decode_static holds";
     default: return "unknown status";
     }
 }
@@ -372,6 +376,50 @@ int santa_device_status(void *workspace, int32_t *code, void *stream)
         return SANTA_ERR_DEVICE;
     }
     return SANTA_OK;
+}
+
+
+// ---------------------------------------------------------------- santa_decode_static
+
+// The scratch buffer of santa_decode_static: a file-scope device array, so that callers
+// that may not allocate device memory can still run a decode step.  Host code must not
+// use its name as an address: the device address comes from cudaGetSymbolAddress, once
+// per device, with that device current.
+static __device__ __align__(256) unsigned char g_static_scratch[SANTA_STATIC_SCRATCH_BYTES];
+
+namespace {
+void *g_static_ptr[santa::MAX_DEV_STATIC];
+}
+
+int santa_decode_static(const santa_shape *shape, const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *seq_lens, int32_t S, int32_t mode, uint64_t seed, float *out,
+                        int32_t *idx_out, void *stream)
+{
+    size_t need = 0;
+    int rc = santa_workspace_size(shape, S, mode, &need);
+    if (rc) return rc;
+    if (need > SANTA_STATIC_SCRATCH_BYTES) return SANTA_ERR_SCRATCH;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SANTA_ERR_CUDA;
+    if (dev < 0 || dev >= santa::MAX_DEV_STATIC) return SANTA_ERR_UNSUPPORTED;
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(santa::g_static_mu);
+        if (!g_static_ptr[dev]) {
+            void *ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return SANTA_ERR_CUDA;
+            g_static_ptr[dev] = ptr;
+        }
+        ws = g_static_ptr[dev];
+    }
+    // the control block (work counters, error word) must start at zero on every call
+    const santa::WsLayout wl = santa::ws_layout(shape->B, shape->H_q, shape->H_kv, shape->d, shape->n_max,
+                                                mode == SANTA_DENSE);
+    const size_t ctrl = santa::align_up(sizeof(int) * (santa::CTRL_GROUPS + (size_t)shape->B * shape->H_kv), 256);
+    if (cudaMemsetAsync(ws, 0, ctrl < wl.total ? ctrl : wl.total, (cudaStream_t)stream) != cudaSuccess)
+        return SANTA_ERR_CUDA;
+    return santa_decode(shape, q, k_cache, v_cache, seq_lens, S, mode, seed, out, idx_out, ws,
+                        SANTA_STATIC_SCRATCH_BYTES, stream);
 }
 
 }  // extern "C"

@@ -22,7 +22,9 @@ DEV_BAD_SEQLEN, DEV_TIMEOUT = 1, 2
 
 # every symbol include/santa.h declares
 EXPORTS = ("santa_workspace_size", "santa_workspace_init", "santa_decode", "santa_sample_points",
-           "santa_device_status", "santa_status_string", "santa_version")
+           "santa_device_status", "santa_status_string", "santa_version", "santa_decode_static")
+ERR_SCRATCH = -7
+STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class SantaError(RuntimeError):
@@ -65,6 +67,8 @@ def load(path: str | None = None):
         lib.santa_device_status.restype = ctypes.c_int
         lib.santa_status_string.argtypes = [ctypes.c_int]
         lib.santa_status_string.restype = ctypes.c_char_p
+        lib.santa_decode_static.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, vp, i32, i32, u64, vp, vp, vp]
+        lib.santa_decode_static.restype = ctypes.c_int
         lib.santa_version.argtypes = []
         lib.santa_version.restype = ctypes.c_int
         _lib = lib
