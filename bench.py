@@ -196,12 +196,12 @@ def run_ours(args):
     idx = torch.empty(B, H_q, S, dtype=torch.int32, device=dev)
     seq = sl.tolist()
 
-    def step_mode(mode, S_=S, seed_box=[0]):
+    def step_mode(mode, S_=S, seed_box=[0], group_dedup=False):
         def f():
             seed_box[0] += 1
             santa.decode(qd, kd, vd, sld, S_, mode, seed=seed_box[0], out=out,
                          idx_out=(idx if mode != "dense" and S_ == S else None),
-                         want_idx=(mode != "dense" and S_ == S))
+                         want_idx=(mode != "dense" and S_ == S), group_dedup=group_dedup)
         return f
 
     peak, peak_kind = measured_peak()
@@ -234,6 +234,15 @@ def run_ours(args):
         al = sum(pm) / len(pm)
         sweep[str(S2)] = {"us_per_step": round(tm * 1000 / extra_steps, 2),
                           "frac_of_peak": round(ab / (al * 1e-3) / 1e9 / peak, 4)}
+
+    # the opt-in group deduplication of V loads (SANTA_GROUP_DEDUP) against the default
+    gdd = {}
+    for S2 in (() if args.no_extras else (256, 2048)):
+        row = {}
+        for flag in (False, True):
+            tm, _ = time_steps(step_mode("systematic", S2, group_dedup=flag), extra_steps, 3, stream, dist)
+            row["group_dedup" if flag else "per_head"] = round(tm * 1000 / extra_steps, 2)
+        gdd[str(S2)] = row
 
     # end to end through the C ABI with host buffers: H2D inputs, decode, D2H result
     e2e = None
@@ -281,6 +290,7 @@ def run_ours(args):
             "clocks": clocks,
             "modes": modes,
             "S_sweep_systematic": sweep,
+            "group_dedup_us_per_step": gdd,
         }
         print(json.dumps(rec), flush=True)
     if dist is not None:

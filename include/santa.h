@@ -49,6 +49,15 @@ extern "C" {
 #define SANTA_SYSTEMATIC 2
 #define SANTA_IID 3
 
+/* Flag, or-ed into a sampling mode: gather each distinct V row once per group of query
+ * heads that share a KV head (the G heads run as one thread-block cluster and exchange
+ * their sample lists), instead of once per head.  It saves V traffic when S is large,
+ * but ties each head's value stage to the slowest head of its group: at S = 256 on the
+ * Llama-shaped batch it is slower, so it is off unless asked for.  It applies when
+ * G > 1 and G * S <= 8192; otherwise it is ignored.  Results agree with the default
+ * to fp32 rounding of the sums. */
+#define SANTA_GROUP_DEDUP 0x100
+
 /* Device error bits (santa_device_status). */
 #define SANTA_DEV_BAD_SEQLEN 1      /* some seq_lens[b] outside [0, n_max]; treated as 0 */
 #define SANTA_DEV_TIMEOUT 2         /* a bounded wait on a shared-memory barrier gave up */
@@ -86,7 +95,8 @@ int santa_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
  *  seq_lens  device int32 [B], each in [0, n_max]; out-of-range values are treated as 0
  *            and set SANTA_DEV_BAD_SEQLEN in the device error word
  *  S         samples per (b, h): 1..4096 (ignored for SANTA_DENSE)
- *  mode      SANTA_DENSE, SANTA_STRATIFIED, SANTA_SYSTEMATIC or SANTA_IID
+ *  mode      SANTA_DENSE, SANTA_STRATIFIED, SANTA_SYSTEMATIC or SANTA_IID, optionally
+ *            or-ed with SANTA_GROUP_DEDUP
  *  seed      Philox4x64-10 key word 0 (ignored for SANTA_DENSE)
  *  out       device fp32 [B, H_q, d]; n_b = 0 gives zeros
  *  idx_out   device int32 [B, H_q, S] or NULL: the sampled key indices of each (b, h),

@@ -18,9 +18,9 @@ int score_smem_bytes(int D, int G, int B)
     return score_smem(D, G, B).total;
 }
 
-int gather_smem_bytes(int D, int S, int nch_used, int mode)
+int gather_smem_bytes(int D, int G, int S, int nch_used, int mode, bool xdedup)
 {
-    return gather_smem(D, S, nch_used, mode).total;
+    return gather_smem(D, G, S, nch_used, mode, xdedup).total;
 }
 
 int dense_smem_bytes(int D, int G, int B)
@@ -165,8 +165,10 @@ int check_shape(const santa_shape *sh)
     return SANTA_OK;
 }
 
-int check_mode_S(int32_t mode, int32_t S)
+int check_mode_S(int32_t mode_flags, int32_t S)
 {
+    if (mode_flags & ~(0xff | SANTA_GROUP_DEDUP)) return SANTA_ERR_INVALID_ARG;
+    const int mode = mode_flags & 0xff;
     if (mode < SANTA_DENSE || mode > SANTA_IID) return SANTA_ERR_INVALID_ARG;
     if (mode != SANTA_DENSE && (S < 1 || S > SMAX)) return SANTA_ERR_INVALID_ARG;
     return SANTA_OK;
@@ -221,7 +223,7 @@ int santa_workspace_size(const santa_shape *shape, int32_t S, int32_t mode, size
     if (rc) return rc;
     if ((rc = check_mode_S(mode, S))) return rc;
     if (!bytes) return SANTA_ERR_INVALID_ARG;
-    *bytes = ws_layout(shape->B, shape->H_q, shape->H_kv, shape->d, shape->n_max, mode == SANTA_DENSE).total;
+    *bytes = ws_layout(shape->B, shape->H_q, shape->H_kv, shape->d, shape->n_max, (mode & 0xff) == SANTA_DENSE).total;
     return SANTA_OK;
 }
 
@@ -241,12 +243,13 @@ int santa_workspace_init(void *workspace, size_t workspace_bytes, void *stream)
 }
 
 int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, const void *v_cache,
-                 const int32_t *seq_lens, int32_t S, int32_t mode, uint64_t seed, float *out, int32_t *idx_out,
+                 const int32_t *seq_lens, int32_t S, int32_t mode_flags, uint64_t seed, float *out, int32_t *idx_out,
                  void *workspace, size_t workspace_bytes, void *stream)
 {
     int rc = check_shape(shape);
     if (rc) return rc;
-    if ((rc = check_mode_S(mode, S))) return rc;
+    if ((rc = check_mode_S(mode_flags, S))) return rc;
+    const int32_t mode = mode_flags & 0xff;
     if (!q || !k_cache || !v_cache || !seq_lens || !out) return SANTA_ERR_INVALID_ARG;
     if (!workspace) return SANTA_ERR_WORKSPACE;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
@@ -311,7 +314,8 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     int smem2 = 0;
     if (!dense) {
         fn2 = (D == 128) ? kernel_d128(KIND_GATHER, G) : kernel_d64(KIND_GATHER, G);
-        smem2 = gather_smem_bytes(D, p.S, p.nch, mode);
+        p.xdedup = ((mode_flags & SANTA_GROUP_DEDUP) && gather_xdedup(G, p.S)) ? 1 : 0;
+        smem2 = gather_smem_bytes(D, G, p.S, p.nch, mode, p.xdedup != 0);
         if (smem2 > optin) return SANTA_ERR_UNSUPPORTED;
         int occ2 = 0;
         if ((rc = prepare_fn(fn2, dev, smem2, &occ2))) return rc;
@@ -325,17 +329,26 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
         cudaSuccess)
         return SANTA_ERR_CUDA;
     if (!dense) {
-        // value stage: one CTA per (b, h_q), a programmatic dependent of the score kernel
+        // value stage: one CTA per (b, h_q), a programmatic dependent of the score kernel;
+        // the G heads of a group form a cluster when they share V loads
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3((unsigned)(shape->B * shape->H_q));
         cfg.blockDim = dim3(NT);
         cfg.dynamicSmemBytes = (size_t)smem2;
         cfg.stream = (cudaStream_t)stream;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+        if (p.xdedup) {
+            // the group's G heads as one thread-block cluster (they share V loads)
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = (unsigned)G;
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.numAttrs = 2;
+        }
         if (cudaLaunchKernelExC(&cfg, fn2, args) != cudaSuccess) return SANTA_ERR_CUDA;
     }
     return SANTA_OK;
@@ -414,7 +427,7 @@ int santa_decode_static(const santa_shape *shape, const void *q, const void *k_c
     }
     // the control block (work counters, error word) must start at zero on every call
     const santa::WsLayout wl = santa::ws_layout(shape->B, shape->H_q, shape->H_kv, shape->d, shape->n_max,
-                                                mode == SANTA_DENSE);
+                                                (mode & 0xff) == SANTA_DENSE);
     const size_t ctrl = santa::align_up(sizeof(int) * (santa::CTRL_GROUPS + (size_t)shape->B * shape->H_kv), 256);
     if (cudaMemsetAsync(ws, 0, ctrl < wl.total ? ctrl : wl.total, (cudaStream_t)stream) != cudaSuccess)
         return SANTA_ERR_CUDA;

@@ -81,6 +81,7 @@ struct Params {
     int B, H_q, H_kv, n_max, n_pad, nch, ns_max;
     int L;            // keys per work unit (sampled path) or split length (dense), multiple of 64
     int S, mode;
+    int xdedup;       // value stage: the group's heads share V loads (thread-block clusters)
     uint64_t seed;
     double rS;        // fp64 value nearest 1/S
     float k2_hi, k2_lo;  // scale*log2(e) as an unevaluated fp32 sum

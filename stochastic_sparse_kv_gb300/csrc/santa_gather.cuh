@@ -24,6 +24,8 @@
 //      and adds it times its count; out = sum / S.
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "santa_sample.cuh"
 
 namespace santa {
@@ -31,13 +33,19 @@ namespace santa {
 constexpr int NCH_SMEM = 4096;  // a head's chunk arrays stay in shared memory up to this many chunks
 constexpr int HCAP = 128;       // hot chunks re-scored per head, at most
 constexpr int HBINS = 256;      // histogram bins that pick the hottest HCAP chunks
+constexpr int XDEDUP_MAX = 8192;  // G * S up to which the group's heads share their V loads
+
+// Whether the value stage can run as clusters of the group's G heads that load each
+// distinct V row once for all of them (on request: SANTA_GROUP_DEDUP; the host then
+// launches clusters of G and sets Params::xdedup).
+__host__ __device__ inline bool gather_xdedup(int G, int S) { return G > 1 && G * S <= XDEDUP_MAX; }
 constexpr int HKCAP = 512;      // heavy keys re-scored per head, at most
 
 struct GatherSmem {
-    int t, O, tot, ce, cm, hot, hv, hvw, hist, idx, acc, qf, misc, total;
+    int t, O, tot, ce, cm, hot, hv, hvw, hist, idx, acc, qf, all, own, recv, misc, total;
 };
 
-__host__ __device__ inline GatherSmem gather_smem(int D, int S, int nch_used, int mode)
+__host__ __device__ inline GatherSmem gather_smem(int D, int G, int S, int nch_used, int mode, bool xd)
 {
     GatherSmem s{};
     const int Sp = (mode == MODE_IID) ? next_pow2(S) : S;
@@ -55,6 +63,9 @@ __host__ __device__ inline GatherSmem gather_smem(int D, int S, int nch_used, in
     s.idx = off; off = (int)align_up((size_t)off + Sp * 4, 16);
     s.acc = off; off += NWARP * D * 4;
     s.qf = off; off += D * 4;
+    s.all = off; off = (int)align_up((size_t)off + (xd ? G * S * 4 : 0), 16);   // the group's G lists
+    s.own = off; off = (int)align_up((size_t)off + (xd ? NWARP * G * D * 4 : 0), 16);  // partial sums
+    s.recv = off; off = (int)align_up((size_t)off + (xd ? G * D * 4 : 0), 16);  // partial sums received
     s.misc = off; off += 32 * 4;
     s.total = (int)align_up((size_t)off, 128);
     return s;
@@ -62,14 +73,15 @@ __host__ __device__ inline GatherSmem gather_smem(int D, int S, int nch_used, in
 
 enum : int { GM_MAX = 0, GM_CMAX = 1, GM_NHOT = 2, GM_NHV = 3, GM_CNT = 4, GM_SCAN = 8 /* NWARP+1 words */ };
 
-template <int D>
-__global__ void __launch_bounds__(NT) santa_gather_kernel(const Params p)
+// (four CTAs per SM: all B*H_q CTAs of a B=16, H_q=32 step fit in one wave)
+template <int D, int G>
+__global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
 {
     constexpr int EPL = D / 32;  // V elements per lane
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned FULL = 0xffffffffu;
-    const int H_q = p.H_q, G = p.H_q / p.H_kv, S = p.S;
+    const int H_q = p.H_q, S = p.S;  // G = H_q / H_kv (template)
     const int bh = blockIdx.x;
     const int b = bh / H_q, h = bh % H_q, g = h / G;
     int n = p.seq_lens[b];
@@ -81,7 +93,7 @@ __global__ void __launch_bounds__(NT) santa_gather_kernel(const Params p)
         return;
     }
     const int nchn = (n + CHUNK - 1) / CHUNK;  // chunks of this sequence
-    const GatherSmem lay = gather_smem(D, S, p.nch, p.mode);
+    const GatherSmem lay = gather_smem(D, G, S, p.nch, p.mode, p.xdedup != 0);
     const bool in_smem = p.nch <= NCH_SMEM;
     const size_t bhc = (size_t)bh * p.nch;
     uint64_t *tfx = reinterpret_cast<uint64_t *>(smem + lay.t);  // points as 64-bit fractions
@@ -340,6 +352,111 @@ __global__ void __launch_bounds__(NT) santa_gather_kernel(const Params p)
     if (p.idx_out)
         for (int s = tid; s < S; s += NT) p.idx_out[(size_t)bh * S + s] = idx[s];
     const uint16_t *vg = p.v + ((size_t)b * p.H_kv + g) * (size_t)p.n_max * D;
+    if constexpr (G > 1) {
+        if (p.xdedup) {
+            // The group's G heads run as one cluster (rank k = head g*G + k).  Each CTA
+            // copies the G sorted lists, loads the distinct rows of its own list that no
+            // lower-ranked head sampled -- so every row of the group is loaded once -- and
+            // adds each, times its count in every head's list, to G partial sums.  The
+            // partial sums meet in their head's CTA and are added in rank order.
+            namespace cg = cooperative_groups;
+            cg::cluster_group cl = cg::this_cluster();
+            const int me = (int)cl.block_rank();
+            int *all = reinterpret_cast<int *>(smem + lay.all);      // [G][S]: every head's list
+            float *red = reinterpret_cast<float *>(smem + lay.own);  // [NWARP][G][D] partial sums
+            float *recv = reinterpret_cast<float *>(smem + lay.recv);  // [G][D]
+            // push this head's sorted list into slot `me` of every CTA of the group
+#pragma unroll
+            for (int k = 0; k < G; ++k) {
+                int *dst = cl.map_shared_rank(all, k) + me * S;
+                for (int s = tid; s < S; s += NT) dst[s] = idx[s];
+            }
+            cl.sync();  // every list is everywhere
+            // each warp takes a run of points of its own list; a point leads if it is the
+            // row's first occurrence here and no lower-ranked head sampled the row
+            const int per = (S + NWARP - 1) / NWARP;
+            const int s0 = min(warp * per, S), s1 = min(s0 + per, S);
+            float acc[G][EPL];
+#pragma unroll
+            for (int k = 0; k < G; ++k)
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[k][e] = 0.f;
+            for (int base = s0; base < s1; base += 32) {
+                const int s = base + lane;
+                const bool in = s < s1;
+                const int j = in ? idx[s] : 0;
+                bool ownr = in && (s == 0 || idx[s - 1] != j);
+                int cnt[G];  // the row's count in each head's list
+#pragma unroll
+                for (int k = 0; k < G; ++k) {
+                    cnt[k] = 0;
+                    if (ownr) {
+                        const int *lk = all + k * S;
+                        const int lo = lower_bound_i(lk, S, j);
+                        cnt[k] = (lo < S && lk[lo] == j) ? upper_bound_i(lk, S, j) - lo : 0;
+                        if (k < me && cnt[k] > 0) ownr = false;  // a lower head loads it
+                    }
+                }
+                unsigned lead = __ballot_sync(FULL, ownr);
+                while (lead) {  // (lead is warp-uniform)
+                    constexpr int U = G <= 4 ? 8 : 4;
+                    int js[U], src[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        src[u] = lead ? __ffs(lead) - 1 : 32;  // 32: no row in this slot
+                        js[u] = __shfl_sync(FULL, j, src[u] & 31);
+                        if (src[u] == 32) js[u] = 0;
+                        lead &= lead - 1u;
+                    }
+                    float vv[U][EPL];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        if constexpr (EPL == 4) {
+                            const uint2 raw = *reinterpret_cast<const uint2 *>(vg + (size_t)js[u] * D + 4 * lane);
+                            vv[u][0] = bf16lo_to_f32(raw.x);
+                            vv[u][1] = bf16hi_to_f32(raw.x);
+                            vv[u][2] = bf16lo_to_f32(raw.y);
+                            vv[u][3] = bf16hi_to_f32(raw.y);
+                        } else {
+                            const uint32_t raw = *reinterpret_cast<const uint32_t *>(vg + (size_t)js[u] * D + 2 * lane);
+                            vv[u][0] = bf16lo_to_f32(raw);
+                            vv[u][1] = bf16hi_to_f32(raw);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+#pragma unroll
+                        for (int k = 0; k < G; ++k) {
+                            const int c = __shfl_sync(FULL, cnt[k], src[u] & 31);
+                            const float cf = src[u] < 32 ? (float)c : 0.f;
+#pragma unroll
+                            for (int e = 0; e < EPL; ++e) acc[k][e] = __fmaf_rn(cf, vv[u][e], acc[k][e]);
+                        }
+                }
+            }
+            // partial sums of this CTA for each head -> slot `me` of that head's CTA
+#pragma unroll
+            for (int k = 0; k < G; ++k)
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) red[(warp * G + k) * D + EPL * lane + e] = acc[k][e];
+            __syncthreads();
+            for (int i = tid; i < G * D; i += NT) {
+                const int k = i / D, dd = i % D;
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < NWARP; ++w) sum = __fadd_rn(sum, red[(w * G + k) * D + dd]);
+                cl.map_shared_rank(recv, k)[me * D + dd] = sum;
+            }
+            cl.sync();  // every partial sum has arrived
+            for (int i = tid; i < D; i += NT) {
+                float sum = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < G; ++jj) sum = __fadd_rn(sum, recv[jj * D + i]);
+                p.out[(size_t)bh * D + i] = __fdiv_rn(sum, (float)S);
+            }
+            return;
+        }
+    }
     const int per = (S + NWARP - 1) / NWARP;
     const int s0 = min(warp * per, S), s1 = min(s0 + per, S);
     float acc[EPL];

@@ -12,7 +12,7 @@ const void *kernel_d128(int kind, int G);
 
 // Dynamic shared-memory bytes of the score, value-stage and dense kernels.
 int score_smem_bytes(int D, int G, int B);
-int gather_smem_bytes(int D, int S, int nch_used, int mode);
+int gather_smem_bytes(int D, int G, int S, int nch_used, int mode, bool xdedup);
 int dense_smem_bytes(int D, int G, int B);
 
 // Device points kernel (santa_sample_points).

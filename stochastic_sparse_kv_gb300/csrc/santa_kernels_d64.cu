@@ -8,7 +8,15 @@ namespace santa {
 
 const void *kernel_d64(int kind, int G)
 {
-    if (kind == KIND_GATHER) return (const void *)santa_gather_kernel<64>;
+    if (kind == KIND_GATHER) {
+        switch (G) {
+        case 1: return (const void *)santa_gather_kernel<64, 1>;
+        case 2: return (const void *)santa_gather_kernel<64, 2>;
+        case 4: return (const void *)santa_gather_kernel<64, 4>;
+        case 8: return (const void *)santa_gather_kernel<64, 8>;
+        }
+        return nullptr;
+    }
     if (kind == KIND_SCORE) {
         switch (G) {
         case 1: return (const void *)santa_score_kernel<64, 1>;

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libsanta.so")
 OK = 0
 DENSE, STRATIFIED, SYSTEMATIC, IID = 0, 1, 2, 3
 MODES = {"dense": DENSE, "stratified": STRATIFIED, "systematic": SYSTEMATIC, "iid": IID}
+GROUP_DEDUP = 0x100  # or-ed into a sampling mode: V rows loaded once per KV-head group
 DEV_BAD_SEQLEN, DEV_TIMEOUT = 1, 2
 
 # every symbol include/santa.h declares
@@ -127,10 +128,11 @@ def _cached_workspace(nbytes: int, device, stream) -> torch.Tensor:
 def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens: torch.Tensor,
            S: int, mode="systematic", seed: int = 0, scale: float = 0.0, out: torch.Tensor | None = None,
            idx_out: torch.Tensor | None = None, want_idx: bool = True, workspace: torch.Tensor | None = None,
-           stream=None):
+           stream=None, group_dedup: bool = False):
     """One SANTA (or dense) decode step on the GPU.  q [B,H_q,d], k/v [B,H_kv,n_max,d] bf16,
     seq_lens [B] int32, all on one CUDA device.  Returns (out fp32 [B,H_q,d],
-    idx int32 [B,H_q,S] or None)."""
+    idx int32 [B,H_q,S] or None).  group_dedup: load each sampled V row once per group of
+    query heads sharing a KV head (SANTA_GROUP_DEDUP)."""
     m = _mode(mode)
     B, H_q, d = q.shape
     _, H_kv, n_max, d2 = k_cache.shape
@@ -149,9 +151,10 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_le
         idx_out = torch.empty(B, H_q, S, dtype=torch.int32, device=dev)
     nbytes = workspace_size(shape, S if m != DENSE else 1, m)
     ws = workspace if workspace is not None else _cached_workspace(nbytes, dev, stream)
+    mf = m | (GROUP_DEDUP if (group_dedup and m != DENSE) else 0)
     rc = load().santa_decode(ctypes.byref(shape), ctypes.c_void_p(q.data_ptr()),
                              ctypes.c_void_p(k_cache.data_ptr()), ctypes.c_void_p(v_cache.data_ptr()),
-                             ctypes.c_void_p(seq_lens.data_ptr()), int(S), m, ctypes.c_uint64(seed),
+                             ctypes.c_void_p(seq_lens.data_ptr()), int(S), mf, ctypes.c_uint64(seed),
                              ctypes.c_void_p(out.data_ptr()),
                              ctypes.c_void_p(idx_out.data_ptr() if (idx_out is not None and m != DENSE) else 0),
                              ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.c_void_p(_stream_ptr(stream)))

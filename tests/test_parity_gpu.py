@@ -59,6 +59,8 @@ CASES = [
     (64, 64, 8, 700, [700, 311], 48),
     # more than 4096 chunks: the value stage keeps its chunk arrays in global memory
     (64, 8, 2, 140000, [140000, 3000], 200),
+    # G * S above the cluster limit: each head gathers its own rows
+    (128, 32, 8, 1500, [1500, 800], 4096),
 ]
 
 
@@ -85,6 +87,30 @@ def test_small_parity(d, H_q, H_kv, n_max, seq, S, mode):
     same = [(b, h) for b in nz for h in range(H_q) if np.array_equal(idx[b, h], i_ref[b, h])]
     sel = tuple(np.array(same).T)
     assert np.abs(o[sel] - o_ref[sel]).max() <= 1e-2
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[2], CASES[3], CASES[5], CASES[6], CASES[8]])
+@pytest.mark.parametrize("mode", ["systematic", "stratified"])
+def test_group_dedup_matches_per_head(case, mode):
+    """SANTA_GROUP_DEDUP: the heads of a KV group load each sampled V row once between
+    them.  Same indices as the default path; outputs equal to fp32 rounding; and the
+    estimator against the oracle's gather of the GPU's indices."""
+    d, H_q, H_kv, n_max, seq, S = case
+    w, q, k, v, sl = workloads.small("gd", len(seq), H_q, H_kv, d, n_max, S, seq_lens=seq, seed=d + H_q + n_max)
+    qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
+    o1, i1 = santa.decode(qd, kd, vd, sld, S, mode, seed=9)
+    o2, i2 = santa.decode(qd, kd, vd, sld, S, mode, seed=9, group_dedup=True)
+    torch.cuda.synchronize()
+    assert torch.equal(i1, i2)
+    assert (o1 - o2).abs().max().item() <= 1e-5
+    idx = i2.cpu().numpy()
+    nz = [b for b in range(len(seq)) if seq[b] > 0]
+    sl1 = torch.tensor([max(x, 1) for x in seq], dtype=torch.int32)
+    ref = oracle.gather(v, sl1, np.where(idx < 0, 0, idx))
+    assert np.abs(o2.cpu().numpy()[nz] - ref[nz]).max() <= 1e-4
+    for b in range(len(seq)):
+        if seq[b] == 0:
+            assert torch.all(o2[b] == 0)
 
 
 @pytest.mark.parametrize("score_std", [0.0, 0.05, 0.5, 1.0, 6.0])

@@ -34,7 +34,8 @@ def _call_workspace(lib, shape, q, k, v, sl, S, mode, seed, out, idx, ws, stream
                             ctypes.c_void_p(stream))
 
 
-@pytest.mark.parametrize("mode", [santa.SYSTEMATIC, santa.STRATIFIED, santa.IID, santa.DENSE])
+@pytest.mark.parametrize("mode", [santa.SYSTEMATIC, santa.STRATIFIED, santa.IID, santa.DENSE,
+                                  santa.SYSTEMATIC | santa.GROUP_DEDUP])
 def test_static_scratch_matches_workspace_entry_point(mode):
     lib = santa.load()
     seq = [3000, 777, 0, 2049]
@@ -45,7 +46,7 @@ def test_static_scratch_matches_workspace_entry_point(mode):
     shape = santa.make_shape(B, H_q, 4, d, 3000)
     stream = torch.cuda.current_stream().cuda_stream
     ws = santa.new_workspace(santa.workspace_size(shape, S, mode), DEV)
-    sampled = mode != santa.DENSE
+    sampled = (mode & 0xff) != santa.DENSE
     for seed in (5, 6):  # two calls in a row, each against the workspace entry point
         out_a = torch.full((B, H_q, d), float("nan"), device=DEV)
         out_b = torch.full((B, H_q, d), float("nan"), device=DEV)
