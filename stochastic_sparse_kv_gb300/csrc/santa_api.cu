@@ -25,7 +25,7 @@ int gather_smem_bytes(int D, int G, int S, int nch_used, int mode, bool xdedup)
 
 int dense_smem_bytes(int D, int G, int B)
 {
-    return dense_smem(D, G, B, 2).total;
+    return dense_smem(D, G, B).total;
 }
 
 // ---------------------------------------------------------------- points kernels
@@ -174,24 +174,6 @@ int check_mode_S(int32_t mode_flags, int32_t S)
     return SANTA_OK;
 }
 
-// Split length of the dense kernel (CTA-wide 64-key tiles): the longest of 1024/512/256
-// keys that still gives every SM at least four work items.
-int choose_L_dense(const santa_shape *sh, int sms)
-{
-    const int cand[3] = {1024, 512, 256};
-    const long long groups = (long long)sh->B * sh->H_kv;
-    int L = 256;
-    for (int i = 0; i < 3; ++i) {
-        const long long ns = (sh->n_max + cand[i] - 1) / cand[i];
-        if (groups * ns >= 4LL * sms) {
-            L = cand[i];
-            break;
-        }
-    }
-    while ((sh->n_max + L - 1) / L > NS_LIMIT) L *= 2;
-    return L;
-}
-
 }  // namespace
 }  // namespace santa
 
@@ -263,7 +245,7 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     int dev, sms, optin;
     if ((rc = device_info(&dev, &sms, &optin))) return rc;
     const int D = shape->d, G = shape->H_q / shape->H_kv;
-    const int L = dense ? choose_L_dense(shape, sms) : UNIT_KEYS;
+    const int L = dense ? DENSE_UNIT : UNIT_KEYS;  // keys per work unit
 
     Params p{};
     uint8_t *ws = static_cast<uint8_t *>(workspace);

@@ -17,7 +17,8 @@ namespace santa {
 constexpr int NT = 256;              // threads per CTA
 constexpr int NWARP = NT / 32;       // 8 warps
 constexpr int UNIT_KEYS = 128;       // keys per work unit of the sampled path's score kernel
-constexpr int LMIN = 128;            // shortest split of the dense kernel
+constexpr int LMIN = 128;            // (tile-size check of the score helpers)
+constexpr int DENSE_UNIT = 512;      // keys per work unit (and per partial) of the dense kernel
 constexpr int CHUNK = 32;            // keys per CDF chunk (one 128-byte line of fp32 w)
 constexpr int NS_LIMIT = 1024;       // most dense splits one sequence may have
 constexpr int NMAX_LIMIT = 524288;   // longest KV cache (keys)
@@ -45,7 +46,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int H_q, int H_kv, int d, i
     WsLayout L{};
     L.n_pad = (int)align_up((size_t)n_max, CHUNK);
     L.nch = L.n_pad / CHUNK;
-    L.ns_max = (n_max + LMIN - 1) / LMIN;
+    L.ns_max = (n_max + DENSE_UNIT - 1) / DENSE_UNIT;  // dense partials per sequence
     const size_t BH = (size_t)B * H_q;
     size_t off = 0;
     L.ctrl = off;

@@ -1,180 +1,232 @@
-// santa_dense.cuh -- dense split-K decode attention (the like-for-like baseline), sm_103a.
+// santa_dense.cuh -- dense decode attention, the like-for-like baseline, sm_103a.
 //
-// Exact softmax attention o = sum_j p_j v_j, the value SANTA estimates ("Stochastic
-// Sparse Attention for Memory-Bound Inference", abstract; the pages' baselines are
-// split-K decode kernels).  The same persistent tile stream and score microkernel as the
-// sampled kernel, but each stage carries the K and the V tile of 64 keys; every warp
-// keeps an online softmax (running max, sum, and G x d partial outputs) over its keys;
-// a split ends with a merge of the 8 warps into one partial (m, l, o) per query head,
-// and the CTA that completes a group merges the group's splits into `out`.
+// Exact softmax attention o = sum_j p_j v_j: the quantity SANTA estimates ("Stochastic
+// Sparse Attention for Memory-Bound Inference", abstract; the pages compare against
+// split-K decode kernels).  Built like the score kernel of the sampled path, so that
+// the comparison is like for like:
+//
+//  * persistent CTAs of 8 independent warps; a warp takes work units of UNIT keys of one
+//    (b, g) -- a static contiguous block first, then shrinking grabs from a counter --
+//    and streams K and V tiles of KEYS keys through its own ring of TMA bulk copies;
+//  * per tile: the G query heads' scores (tile_dots), an online softmax per head (running
+//    maximum m and sum l in log2 units, with rescaling when m grows), and p.V with the
+//    tile's probabilities broadcast through shared memory; each lane owns D/32 output
+//    dimensions of every head;
+//  * at the end of a unit the warp writes its partial (m, l, o) per head; the warp that
+//    completes the last unit of a group merges the group's partials into `out`.
 #pragma once
 
 #include "santa_sample.cuh"
 
 namespace santa {
 
-struct DenseSmem {
-    int stage, bar, desc, misc, nb, prefix, pbuf, merge, total;
+template <int D, int G>
+struct DenseTile {
+    static constexpr int KEYS = (D == 128) ? 16 : 32;  // keys per tile (a multiple of tile_dots' KW)
+    static constexpr int KVB = KEYS * 2 * D;           // bytes of the tile's K (or V) part: 4 KB
+    static constexpr int NSTAGE = 3;
+    static constexpr int QBYTES = G * D * 2;
+    static constexpr int UNIT = DENSE_UNIT;            // keys per work unit
+    static constexpr int EPL = D / 32;                 // output dimensions per lane
 };
 
-__host__ __device__ inline DenseSmem dense_smem(int D, int G, int B, int nstage)
+struct DenseSmem {
+    int nb, prefix, misc, warp0, warp_bytes, ring, qbuf, pbuf, bar, desc, total;
+};
+
+__host__ __device__ inline DenseSmem dense_smem(int D, int G, int B)
 {
+    const int keys = (D == 128) ? 16 : 32;
+    const int kvb = keys * 2 * D;
+    const int nstage = 3;
     DenseSmem s{};
-    const int P = D / 16, KW = 64 / P;
     int off = 0;
-    s.stage = off; off += nstage * 2 * TILE_BYTES;
-    s.bar = off; off += nstage * 8;
-    s.desc = off; off += nstage * 16;
-    s.misc = off; off += 16 * 4;
     s.nb = off; off += (int)align_up((size_t)B * 4, 16);
     s.prefix = off; off += (int)align_up((size_t)(B + 1) * 4, 16);
-    s.pbuf = off; off += NWARP * KW * G * 8;
-    off = (int)align_up((size_t)off, 16);
-    s.merge = off; off += NWARP * G * D * 4 + NWARP * G * 2 * 4;
-    s.total = off;
+    s.misc = off; off += 16 * 4;
+    s.warp0 = (int)align_up((size_t)off, 128);
+    int w = 0;
+    s.ring = w; w += nstage * 2 * kvb;
+    s.qbuf = w; w += G * D * 2;
+    s.pbuf = w; w += keys * G * 4 + G * 4;  // the tile's p[key][head], then alpha[head]
+    s.bar = w = (int)align_up((size_t)w, 8); w += nstage * 8;
+    s.desc = w = (int)align_up((size_t)w, 16); w += nstage * 16;
+    s.warp_bytes = (int)align_up((size_t)w, 128);
+    s.total = s.warp0 + NWARP * s.warp_bytes;
     return s;
 }
 
 template <int D, int G>
-struct DenseCfg {
-    using C = SampleCfg<D, G>;
-    static constexpr int NSTAGE = 2;
-    static constexpr int NPAIR = C::EPL / 2;   // output fp32 pairs per lane and head
-    // a lane and slot that hold head h after the score reduction
-    __host__ __device__ static constexpr int rep_lane(int h)
-    {
-        for (int l = 0; l < 32; ++l)
-            for (int i = 0; i < C::NV; ++i)
-                if (C::head_of(l, i) == h) return l;
-        return 0;
-    }
-    __host__ __device__ static constexpr int rep_slot(int h)
-    {
-        for (int l = 0; l < 32; ++l)
-            for (int i = 0; i < C::NV; ++i)
-                if (C::head_of(l, i) == h) return i;
-        return 0;
-    }
-    // both packed per head (lane in bits 0-7, slot above), evaluated by the compiler
-    __host__ __device__ static constexpr unsigned long long rep_table()
-    {
-        unsigned long long t = 0;
-        for (int h = 0; h < G; ++h)
-            t |= (unsigned long long)(rep_lane(h) | (rep_slot(h) << 5)) << (8 * h);
-        return t;
-    }
-    static constexpr unsigned long long REP = rep_table();
-    __host__ __device__ static constexpr int lane_of(int h) { return (int)((REP >> (8 * h)) & 31); }
-    __host__ __device__ static constexpr int slot_of(int h) { return (int)((REP >> (8 * h + 5)) & 7); }
-};
-
-template <int D, int G>
-__global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_dense_kernel(const Params p)
+__global__ void __launch_bounds__(NT, 1) santa_dense_kernel(const Params p)
 {
     using C = SampleCfg<D, G>;
-    using DC = DenseCfg<D, G>;
-    constexpr int NSTAGE = DC::NSTAGE;
+    using T = DenseTile<D, G>;
+    constexpr int NSTAGE = T::NSTAGE;
+    constexpr int NCALL = T::KEYS / C::KW;  // tile_dots calls per tile
+    constexpr int NV = C::NV;
+    constexpr int EPL = T::EPL;
+    constexpr int L = T::UNIT;
+    constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sub = lane % C::P, grp = lane / C::P;
-    const int B = p.B, H_kv = p.H_kv, H_q = p.H_q, L = p.L;
-    const DenseSmem lay = dense_smem(D, G, B, NSTAGE);
-
-    uint8_t *stage = smem + lay.stage;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + lay.bar);
-    int4 *sdesc = reinterpret_cast<int4 *>(smem + lay.desc);
-    int *misc = reinterpret_cast<int *>(smem + lay.misc);
+    const int B = p.B, H_kv = p.H_kv, H_q = p.H_q;
+    const DenseSmem lay = dense_smem(D, G, B);
     int *nb = reinterpret_cast<int *>(smem + lay.nb);
     int *prefix = reinterpret_cast<int *>(smem + lay.prefix);
-    unsigned long long *pbuf = reinterpret_cast<unsigned long long *>(smem + lay.pbuf);
-    float *mg_o = reinterpret_cast<float *>(smem + lay.merge);
-    float *mg_ml = mg_o + NWARP * G * D;
+    int *misc = reinterpret_cast<int *>(smem + lay.misc);
+    uint8_t *wb = smem + lay.warp0 + warp * lay.warp_bytes;
+    uint8_t *ring = wb + lay.ring;
+    uint8_t *qbuf = wb + lay.qbuf;
+    float *pk = reinterpret_cast<float *>(wb + lay.pbuf);  // [KEYS][G], then alpha[G]
+    float *alpha_s = pk + T::KEYS * G;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(wb + lay.bar);
+    int4 *desc = reinterpret_cast<int4 *>(wb + lay.desc);
     const float NEG_INF = __int_as_float(0xff800000);
 
-    build_item_space(p, nb, prefix, misc);
-    if (tid == 0) {
+    // the work units: UNIT keys per (b, g, r), counted per batch row like the score kernel's
+    Params pu = p;
+    pu.L = L;
+    build_item_space(pu, nb, prefix, misc);
+    if (lane == 0) {
         for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
         mbar_fence_init();
     }
-    __syncthreads();
+    __syncthreads();  // the only CTA-wide barrier
     const int total_items = prefix[B];
+    const int W = (int)gridDim.x * NWARP;
+    const int gw = (int)blockIdx.x * NWARP + warp;
+    const int Ks = (int)((long long)total_items * 4 / 5 / W);  // static units per warp
+    const int dyn0 = Ks * W;
 
-    int pr_item = 0, pr_tile = 0, pr_ntiles = 0, pr_valid = 0, pr_next = 0;
+    // ---- producer (warp-uniform; lane 0 issues the copies and the atomics)
+    uint64_t policy = 0;
+    int pend = 0;  // lane 0: the outstanding grab, first unit * 8 + size
+    auto request = [&](int last) {
+        if (lane == 0) {
+            const int k = max(1, min(4, (total_items - last) / (2 * W)));
+            pend = (dyn0 + atomicAdd(p.ctrl + CTRL_WORK, k)) * 8 + k;
+        }
+    };
+    if (lane == 0) policy = l2_policy_evict_first();
+    request(dyn0);
+    int g_next = gw * Ks, g_end = g_next + Ks;  // the current grab: the static block first
+    int pr_r = 0, pr_tile = 0, pr_ntiles = 0, pr_valid = 0, pr_grp = 0, pr_group = -1, pr_seq = 0;
+    int q_issue = -1;  // sequence number of the tile that carried the staged query heads
     long long pr_row0 = 0;
     bool pr_end = false;
-    uint64_t policy = 0;
-    if (tid == 0) {
-        policy = l2_policy_evict_first();
-        pr_next = atomicAdd(p.ctrl + CTRL_WORK, 1);
-    }
-    auto produce = [&](int slot) {
-        if (!pr_end && pr_tile == pr_ntiles) {
-            const int it = pr_next;
-            if (it < 0 || it >= total_items) {
-                pr_end = true;
-            } else {
-                pr_next = atomicAdd(p.ctrl + CTRL_WORK, 1);
-                const Item x = decode_item(it, prefix, nb, B, H_kv, L);
-                pr_item = it;
-                pr_tile = 0;
-                if (x.n == 0) {
-                    pr_ntiles = 0;
-                    sdesc[slot] = make_int4(it, 0, 0, FLAG_ZERO);
-                    mbar_arrive(&bars[slot]);
-                    return;
-                }
-                pr_valid = min(L, x.n - x.r * L);
-                pr_ntiles = (pr_valid + C::TK - 1) / C::TK;
-                pr_row0 = ((long long)x.b * H_kv + x.g) * p.n_max + (long long)x.r * L;
+    int ub = 0, ug = 0, ur = 0, uns = 1;  // position of unit g_next
+    auto seek = [&](int itm) {
+        const Item x = decode_item(itm, prefix, nb, B, H_kv, L);
+        ub = x.b;
+        ug = x.g;
+        ur = x.r;
+        uns = x.ns;
+    };
+    auto step = [&]() {
+        if (++ur == uns) {
+            ur = 0;
+            if (++ug == H_kv) {
+                ug = 0;
+                if (++ub < B) uns = nb[ub] > 0 ? (nb[ub] + L - 1) / L : 1;
             }
         }
+    };
+    if (g_next < g_end) seek(g_next);
+    auto produce = [&](int slot, int cons_seq) {
+        while (!pr_end && pr_tile == pr_ntiles) {
+            if (g_next == g_end) {
+                const int got = __shfl_sync(FULL, pend, 0);
+                g_next = got >> 3;
+                g_end = min(g_next + (got & 7), total_items);
+                if (g_next >= total_items) {
+                    pr_end = true;
+                    break;
+                }
+                request(g_end);
+                seek(g_next);
+            }
+            const int n = nb[ub];
+            const int b = ub, g = ug, r = ur;
+            ++g_next;
+            step();
+            if (n == 0) {  // an empty sequence: its group's outputs are zero
+                float *o = p.out + ((size_t)b * H_q + (size_t)g * G) * D;
+                for (int i = lane; i < G * D; i += 32) o[i] = 0.f;
+                continue;
+            }
+            pr_r = r;
+            pr_tile = 0;
+            pr_valid = min(L, n - r * L);
+            pr_ntiles = (pr_valid + T::KEYS - 1) / T::KEYS;
+            pr_grp = b * H_kv + g;
+            pr_row0 = (long long)pr_grp * p.n_max + (long long)r * L;
+        }
         if (pr_end) {
-            sdesc[slot] = make_int4(DESC_END, 0, 0, 0);
-            mbar_arrive(&bars[slot]);
+            if (lane == 0) desc[slot] = make_int4(DESC_END, 0, 0, 0);
             return;
         }
-        const int rows = min(C::TK, pr_valid - pr_tile * C::TK);
-        const int flags = (pr_tile == pr_ntiles - 1) ? FLAG_LAST : 0;
-        sdesc[slot] = make_int4(pr_item, pr_tile, rows, flags);
-        const uint32_t bytes = (uint32_t)rows * C::ROWB;
-        const long long row = pr_row0 + (long long)pr_tile * C::TK;
-        mbar_arrive_tx(&bars[slot], 2 * bytes);
-        bulk_g2s(stage + slot * 2 * TILE_BYTES, p.k + row * D, bytes, &bars[slot], policy);
-        bulk_g2s(stage + slot * 2 * TILE_BYTES + TILE_BYTES, p.v + row * D, bytes, &bars[slot], policy);
+        const int rows = min(T::KEYS, pr_valid - pr_tile * T::KEYS);
+        int flags = (pr_tile == pr_ntiles - 1) ? TF_LAST : 0;
+        uint32_t qbytes = 0;
+        if (pr_tile == 0 && pr_grp != pr_group) {
+            pr_group = pr_grp;
+            flags |= TF_NEWQ;
+            // the staging buffer is free once the consumer has started the tile that carried it
+            if (q_issue <= cons_seq) {
+                q_issue = pr_seq;
+                qbytes = T::QBYTES;
+            } else {
+                flags |= TF_QGLOBAL;
+            }
+        }
+        if (lane == 0) {
+            desc[slot] = make_int4(pr_grp, (pr_r << 8) | pr_tile, rows, flags);
+            const uint32_t bytes = (uint32_t)rows * C::ROWB;
+            const long long row = pr_row0 + (long long)pr_tile * T::KEYS;
+            uint8_t *dst = ring + slot * 2 * T::KVB;
+            mbar_arrive_tx(&bars[slot], 2 * bytes + qbytes);
+            bulk_g2s(dst, p.k + row * D, bytes, &bars[slot], policy);
+            bulk_g2s(dst + T::KVB, p.v + row * D, bytes, &bars[slot], policy);
+            if (qbytes) bulk_g2s_plain(qbuf, p.q + (size_t)pr_grp * G * D, qbytes, &bars[slot]);
+        }
         ++pr_tile;
+        ++pr_seq;
     };
-    if (tid == 0)
-        for (int s = 0; s < NSTAGE; ++s) produce(s);
+    for (int s = 0; s < NSTAGE; ++s) produce(s, -1);
 
+    // ---- consumer
     unsigned long long qp[G][8];
-    float m_w[G];                       // running maximum per head (log2 units), warp-uniform
-    float l_l[C::NV];                   // this lane's share of the running sum, per score slot
-    unsigned long long o2[G][DC::NPAIR];  // output partials: lane's EPL elements per head
-    Item cur{0, 0, 0, 0, 1};
+    float m[NV], l[NV];   // per score slot (head): running maximum (log2 units) and sum
+    float acc[G][EPL];    // this lane's output dimensions of every head
+    auto reset_unit = [&]() {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            m[i] = NEG_INF;
+            l[i] = 0.f;
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
+    };
+    reset_unit();
+    const bool own = (sub % C::REP) == 0;
     bool aborted = false;
     int it = 0;
-
     for (;; ++it) {
         const int slot = it % NSTAGE;
-        const uint32_t par = (uint32_t)(it / NSTAGE) & 1u;
-        const bool ok = mbar_wait_bounded(&bars[slot], par, p.wait_ns);
-        if (__syncthreads_or(!ok)) {
+        __syncwarp();
+        const int4 dsc = desc[slot];
+        if (dsc.x == DESC_END) break;
+        if (!mbar_wait_bounded(&bars[slot], (uint32_t)(it / NSTAGE) & 1u, p.wait_ns)) {
             aborted = true;
             break;
         }
-        const int4 dsc = sdesc[slot];
-        if (dsc.x == DESC_END) break;
-        if (dsc.w & FLAG_ZERO) {
-            const Item x = decode_item(dsc.x, prefix, nb, B, H_kv, L);
-            for (int i = tid; i < G * D; i += NT) p.out[((size_t)x.b * H_q + x.g * G) * D + i] = 0.f;
-            __syncthreads();
-            if (tid == 0) produce(slot);
-            continue;
-        }
-        const int tile = dsc.y, rows = dsc.z;
-        if (tile == 0) {
-            cur = decode_item(dsc.x, prefix, nb, B, H_kv, L);
-            const uint16_t *qg = p.q + ((size_t)cur.b * H_q + (size_t)cur.g * G) * D;
+        const int grpid = dsc.x, ur_c = dsc.y >> 8, rows = dsc.z, flags = dsc.w;
+        if (flags & TF_NEWQ) {
+            const uint16_t *qg = (flags & TF_QGLOBAL) ? p.q + (size_t)grpid * G * D
+                                                       : reinterpret_cast<const uint16_t *>(qbuf);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 const uint4 a = *reinterpret_cast<const uint4 *>(qg + h * D + 8 * sub);
@@ -182,176 +234,166 @@ __global__ void __launch_bounds__(NT, (G <= 4 ? 2 : 1)) santa_dense_kernel(const
                 const uint32_t wv[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) qp[h][i] = bf16x2_to_f32x2(wv[i]);
-                m_w[h] = NEG_INF;
-#pragma unroll
-                for (int j = 0; j < DC::NPAIR; ++j) o2[h][j] = 0ull;
-            }
-#pragma unroll
-            for (int i = 0; i < C::NV; ++i) l_l[i] = 0.f;
-        }
-        const uint8_t *kt = stage + slot * 2 * TILE_BYTES;
-        const uint8_t *vt = kt + TILE_BYTES;
-        const int kwarp = warp * C::KW;
-        const int kbase = kwarp + 2 * grp;
-        float val[2 * G];
-        tile_dots<D, G>(kt, kbase, sub, qp, val);
-        float s2[C::NV];
-#pragma unroll
-        for (int i = 0; i < C::NV; ++i) {
-            const int key = kbase + C::key2_of(lane, i);
-            s2[i] = key < rows ? __fmul_rn(val[i], p.k2_hi) : NEG_INF;
-        }
-        float wm[C::NV];
-#pragma unroll
-        for (int i = 0; i < C::NV; ++i) wm[i] = s2[i];
-#pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-            if (C::SAME & (unsigned)m) {
-#pragma unroll
-                for (int i = 0; i < C::NV; ++i) wm[i] = fmaxf(wm[i], __shfl_xor_sync(0xffffffffu, wm[i], m));
             }
         }
-        float m_new[G], alpha[G];
+        const uint8_t *kt = ring + slot * 2 * T::KVB;
+        const uint8_t *vt = kt + T::KVB;
+
+        // ---- scores, then the online softmax step of every head
+        float sc[NCALL][NV];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float mt = __shfl_sync(0xffffffffu, wm[DC::slot_of(h)], DC::lane_of(h));
-            m_new[h] = fmaxf(m_w[h], mt);
-            alpha[h] = (m_new[h] == NEG_INF) ? 1.f : exp2f(m_w[h] - m_new[h]);
-            m_w[h] = m_new[h];
-            const unsigned long long a2 = f32x2_pack(alpha[h], alpha[h]);
+        for (int c = 0; c < NCALL; ++c) {
+            float val[2 * G];
+            tile_dots<D, G>(kt, c * C::KW + 2 * grp, sub, qp, val);
 #pragma unroll
-            for (int j = 0; j < DC::NPAIR; ++j) o2[h][j] = fmul2(o2[h][j], a2);
+            for (int i = 0; i < NV; ++i) sc[c][i] = val[i];
         }
-        unsigned long long *pw = pbuf + warp * C::KW * G;
 #pragma unroll
-        for (int i = 0; i < C::NV; ++i) {
+        for (int i = 0; i < NV; ++i) {
+            float tm = NEG_INF;
+#pragma unroll
+            for (int c = 0; c < NCALL; ++c) {
+                const int key = c * C::KW + 2 * grp + C::key2_of(lane, i);
+                if (key < rows) tm = fmaxf(tm, __fmul_rn(sc[c][i], p.k2_hi));
+            }
+#pragma unroll
+            for (int msk = 1; msk < 32; msk <<= 1)
+                if (C::SAME & (unsigned)msk) tm = fmaxf(tm, __shfl_xor_sync(FULL, tm, msk));
+            const float mn = fmaxf(m[i], tm);
+            const float al = exp2f(m[i] - mn);  // 0 on the unit's first tile
             const int h = C::head_of(lane, i);
-            float mh = m_new[0], ah = alpha[0];
+            float ps = 0.f;
 #pragma unroll
-            for (int hh = 1; hh < G; ++hh) {
-                mh = (h == hh) ? m_new[hh] : mh;
-                ah = (h == hh) ? alpha[hh] : ah;
+            for (int c = 0; c < NCALL; ++c) {
+                const int key = c * C::KW + 2 * grp + C::key2_of(lane, i);
+                if (key < rows && own) {
+                    const float pv = exp2f(__fmaf_rn(sc[c][i], p.k2_lo, __fmaf_rn(sc[c][i], p.k2_hi, -mn)));
+                    pk[key * G + h] = pv;
+                    ps = __fadd_rn(ps, pv);
+                }
             }
-            const float pr = (s2[i] == NEG_INF) ? 0.f : exp2f(s2[i] - mh);
-            const bool own = (sub % C::REP) == 0;
-            l_l[i] = __fmaf_rn(l_l[i], ah, own ? pr : 0.f);
-            if (own) pw[(2 * grp + C::key2_of(lane, i)) * G + h] = f32x2_pack(pr, pr);
+#pragma unroll
+            for (int msk = 1; msk < 32; msk <<= 1)
+                if (C::SAME & (unsigned)msk) ps = __fadd_rn(ps, __shfl_xor_sync(FULL, ps, msk));
+            l[i] = __fmaf_rn(l[i], al, ps);
+            m[i] = mn;
+            if ((lane & C::SAME) == 0 && own) alpha_s[h] = al;
         }
         __syncwarp();
-        const int nk = min(C::KW, rows - kwarp);
-        for (int key = 0; key < nk; ++key) {
-            const uint8_t *vrow = vt + (kwarp + key) * C::ROWB;
-            unsigned long long vp[DC::NPAIR];
-            if constexpr (C::EPL == 4) {
-                const uint2 raw = *reinterpret_cast<const uint2 *>(vrow + 8 * lane);
-                vp[0] = bf16x2_to_f32x2(raw.x);
-                vp[1] = bf16x2_to_f32x2(raw.y);
+
+        // ---- p.V: rescale, then add the tile's rows (this lane's EPL dimensions)
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float a = alpha_s[h];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[h][e] = __fmul_rn(acc[h][e], a);
+        }
+        auto add_row = [&](int k) {
+            float pv[G];
+            if constexpr (G % 4 == 0) {
+#pragma unroll
+                for (int h4 = 0; h4 < G; h4 += 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(pk + k * G + h4);
+                    pv[h4] = x.x;
+                    pv[h4 + 1] = x.y;
+                    pv[h4 + 2] = x.z;
+                    pv[h4 + 3] = x.w;
+                }
             } else {
-                const uint32_t raw = *reinterpret_cast<const uint32_t *>(vrow + 4 * lane);
-                vp[0] = bf16x2_to_f32x2(raw);
+#pragma unroll
+                for (int h = 0; h < G; ++h) pv[h] = pk[k * G + h];
             }
+            float vv[EPL];
+            if constexpr (EPL == 4) {
+                const uint2 raw = *reinterpret_cast<const uint2 *>(vt + k * C::ROWB + 8 * lane);
+                vv[0] = bf16lo_to_f32(raw.x);
+                vv[1] = bf16hi_to_f32(raw.x);
+                vv[2] = bf16lo_to_f32(raw.y);
+                vv[3] = bf16hi_to_f32(raw.y);
+            } else {
+                const uint32_t raw = *reinterpret_cast<const uint32_t *>(vt + k * C::ROWB + 4 * lane);
+                vv[0] = bf16lo_to_f32(raw);
+                vv[1] = bf16hi_to_f32(raw);
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[h][e] = __fmaf_rn(pv[h], vv[e], acc[h][e]);
+        };
+        if (rows == T::KEYS) {  // full tiles: unrolled
+#pragma unroll
+            for (int k = 0; k < T::KEYS; ++k) add_row(k);
+        } else {
+            for (int k = 0; k < rows; ++k) add_row(k);
+        }
+        __syncwarp();
+        produce(slot, it);  // K, V and the query heads are consumed: refill the slot
+
+        // ---- end of a unit: its partial (m, l, o) per head; the last unit of a group merges
+        if (flags & TF_LAST) {
+            const size_t bh0 = (size_t)grpid * G;  // first query head of the group
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+                if ((lane & C::SAME) == 0 && own) {
+                    const size_t at = ((bh0 + C::head_of(lane, i)) * p.ns_max + ur_c) * 2;
+                    p.dpart_ml[at] = m[i];
+                    p.dpart_ml[at + 1] = l[i];
+                }
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const unsigned long long pp = pw[key * G + h];
+                float *o = p.dpart_o + ((bh0 + h) * p.ns_max + ur_c) * D + EPL * lane;
 #pragma unroll
-                for (int j = 0; j < DC::NPAIR; ++j) ffma2(o2[h][j], vp[j], pp);
+                for (int e = 0; e < EPL; ++e) o[e] = acc[h][e];
             }
-        }
-        __syncthreads();
-        if (tid == 0) produce(slot);
-
-        if (!(dsc.w & FLAG_LAST)) continue;
-
-        // ================= end of split: merge the warps into (m, l, o) per head
-        const int b = cur.b, g = cur.g, r = cur.r;
-        {
-            float lsum[C::NV];
+            reset_unit();
+            __threadfence();
+            __syncwarp();
+            int done = 0;
+            if (lane == 0) done = atomicAdd(p.ctrl + CTRL_GROUPS + grpid, 1) + 1;
+            done = __shfl_sync(FULL, done, 0);
+            const int nsg = (nb[grpid / H_kv] + L - 1) / L;
+            if (done == nsg) {
+                __threadfence();
+                for (int h = 0; h < G; ++h) {
+                    const size_t base = (bh0 + h) * p.ns_max;
+                    float M = NEG_INF;
+                    for (int u = lane; u < nsg; u += 32) M = fmaxf(M, __ldcg(p.dpart_ml + (base + u) * 2));
 #pragma unroll
-            for (int i = 0; i < C::NV; ++i) lsum[i] = l_l[i];
+                    for (int msk = 16; msk >= 1; msk >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, msk));
+                    float o[EPL], lsum = 0.f;
 #pragma unroll
-            for (int m = 1; m < 32; m <<= 1) {
-                if (C::SAME & (unsigned)m) {
+                    for (int e = 0; e < EPL; ++e) o[e] = 0.f;
+#pragma unroll 4
+                    for (int u = 0; u < nsg; ++u) {
+                        const float f = exp2f(__ldcg(p.dpart_ml + (base + u) * 2) - M);
+                        lsum = __fmaf_rn(f, __ldcg(p.dpart_ml + (base + u) * 2 + 1), lsum);
+                        const float *ou = p.dpart_o + (base + u) * D + EPL * lane;
 #pragma unroll
-                    for (int i = 0; i < C::NV; ++i) lsum[i] = __fadd_rn(lsum[i], __shfl_xor_sync(0xffffffffu, lsum[i], m));
+                        for (int e = 0; e < EPL; ++e) o[e] = __fmaf_rn(f, __ldcg(ou + e), o[e]);
+                    }
+                    float *dst = p.out + (bh0 + h) * D + EPL * lane;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) dst[e] = __fdiv_rn(o[e], lsum);
                 }
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float lh = __shfl_sync(0xffffffffu, lsum[DC::slot_of(h)], DC::lane_of(h));
-                if (lane == 0) {
-                    mg_ml[(warp * G + h) * 2] = m_w[h];
-                    mg_ml[(warp * G + h) * 2 + 1] = lh;
-                }
-#pragma unroll
-                for (int j = 0; j < DC::NPAIR; ++j) {
-                    const float2 f = f32x2_unpack(o2[h][j]);
-                    mg_o[(warp * G + h) * D + C::EPL * lane + 2 * j] = f.x;
-                    mg_o[(warp * G + h) * D + C::EPL * lane + 2 * j + 1] = f.y;
-                }
+                if (lane == 0) p.ctrl[CTRL_GROUPS + grpid] = 0;  // ready for the next call
             }
         }
-        __syncthreads();
-        for (int i = tid; i < G * D; i += NT) {
-            const int h = i / D, dd = i % D;
-            float M = NEG_INF;
-#pragma unroll
-            for (int w = 0; w < NWARP; ++w) M = fmaxf(M, mg_ml[(w * G + h) * 2]);
-            float o = 0.f, l = 0.f;
-#pragma unroll
-            for (int w = 0; w < NWARP; ++w) {
-                const float mw = mg_ml[(w * G + h) * 2];
-                if (mw == NEG_INF) continue;
-                const float f = exp2f(mw - M);
-                o = __fmaf_rn(mg_o[(w * G + h) * D + dd], f, o);
-                l = __fmaf_rn(mg_ml[(w * G + h) * 2 + 1], f, l);
-            }
-            const size_t bh = (size_t)b * H_q + g * G + h;
-            p.dpart_o[(bh * p.ns_max + r) * D + dd] = o;
-            if (dd == 0) {
-                p.dpart_ml[(bh * p.ns_max + r) * 2] = M;
-                p.dpart_ml[(bh * p.ns_max + r) * 2 + 1] = l;
-            }
-        }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            const int prev = atomicAdd(p.ctrl + CTRL_GROUPS + b * H_kv + g, 1);
-            misc[MISC_LAST] = (prev == cur.ns - 1) ? 1 : 0;
-        }
-        __syncthreads();
-        if (!misc[MISC_LAST]) continue;
-        __threadfence();
-        // ================= group epilogue: log-sum-exp merge of the splits
-        const int ns = cur.ns;
-        for (int i = tid; i < G * D; i += NT) {
-            const int h = i / D, dd = i % D;
-            const size_t bh = (size_t)b * H_q + g * G + h;
-            float M = NEG_INF;
-            for (int rr = 0; rr < ns; ++rr) M = fmaxf(M, __ldcg(p.dpart_ml + (bh * p.ns_max + rr) * 2));
-            float o = 0.f, l = 0.f;
-            for (int rr = 0; rr < ns; ++rr) {
-                const float mr = __ldcg(p.dpart_ml + (bh * p.ns_max + rr) * 2);
-                if (mr == NEG_INF) continue;
-                const float f = exp2f(mr - M);
-                o = __fmaf_rn(__ldcg(p.dpart_o + (bh * p.ns_max + rr) * D + dd), f, o);
-                l = __fmaf_rn(__ldcg(p.dpart_ml + (bh * p.ns_max + rr) * 2 + 1), f, l);
-            }
-            p.out[bh * D + dd] = __fdiv_rn(o, l);
-        }
-        if (tid == 0) p.ctrl[CTRL_GROUPS + b * H_kv + g] = 0;
-        __syncthreads();
     }
 
     if (aborted) {
-        if (tid == 0) {
+        // give the copies still in flight a bounded chance to land before the CTA exits
+        if (lane == 0) {
             set_dev_error(p.ctrl, DEV_TIMEOUT);
             for (int k = 0; k < NSTAGE; ++k) {
                 const int j = it + k;
-                mbar_wait_bounded(&bars[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u, p.wait_ns);
+                if (desc[j % NSTAGE].x != DESC_END)
+                    mbar_wait_bounded(&bars[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u, p.wait_ns);
             }
         }
-        __syncthreads();
+        __syncwarp();
     }
+    __threadfence();
+    __syncthreads();
     if (tid == 0) {
         const int done = atomicAdd(p.ctrl + CTRL_EXIT, 1);
         if (done == (int)gridDim.x - 1) {

@@ -58,9 +58,12 @@ __host__ __device__ inline int next_pow2(int x)
     return p;
 }
 
-// Descriptor of a staged tile.
+// Descriptor of a staged tile (int4: group b*H_kv+g, (unit << 8) | tile, rows, flags).
 enum : int { DESC_END = -1 };
-enum : int { FLAG_LAST = 1, FLAG_ZERO = 2 };
+// Flags: the tile is the first of a new (b, g), whose query heads come in staging buffer
+// (flags >> TF_QB_SHIFT) & 1, or must be read from global memory; the tile is the last
+// of its work unit.
+enum : int { TF_NEWQ = 1, TF_QGLOBAL = 2, TF_QB_SHIFT = 2, TF_LAST = 8 };
 
 struct Item {
     int b, g, r, n, ns;

@@ -72,9 +72,6 @@ __host__ __device__ inline ScoreSmem score_smem(int D, int G, int B)
     return s;
 }
 
-// Tile descriptor flags (int4.w): the tile is the first of a new (b, g); its query heads
-// come in staging buffer (flags >> TF_QB_SHIFT) & 1, or are read from global memory.
-enum : int { TF_NEWQ = 1, TF_QGLOBAL = 2, TF_QB_SHIFT = 2 };
 
 template <int D, int G>
 __global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
