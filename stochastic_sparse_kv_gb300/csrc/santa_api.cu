@@ -174,6 +174,18 @@ int check_mode_S(int32_t mode_flags, int32_t S)
     return SANTA_OK;
 }
 
+// Keys per work unit of the sampled path's score kernel: 128, or 64 or 32 when the
+// problem has too few 128-key units to keep every warp (NWARP per SM) busy to the end.
+int choose_unit_sampled(const santa_shape *sh, int sms)
+{
+    const long long warps = (long long)sms * NWARP;
+    for (int L = UNIT_KEYS; L > CHUNK; L /= 2) {
+        const long long units = (long long)sh->B * sh->H_kv * ((sh->n_max + L - 1) / L);
+        if (units >= 4 * warps) return L;
+    }
+    return CHUNK;
+}
+
 }  // namespace
 }  // namespace santa
 
@@ -245,7 +257,7 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     int dev, sms, optin;
     if ((rc = device_info(&dev, &sms, &optin))) return rc;
     const int D = shape->d, G = shape->H_q / shape->H_kv;
-    const int L = dense ? DENSE_UNIT : UNIT_KEYS;  // keys per work unit
+    const int L = dense ? DENSE_UNIT : choose_unit_sampled(shape, sms);  // keys per work unit
 
     Params p{};
     uint8_t *ws = static_cast<uint8_t *>(workspace);

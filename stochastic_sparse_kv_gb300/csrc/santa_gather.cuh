@@ -20,8 +20,9 @@
 //      boundary;
 //   E. the exact exclusive prefix O_c of the G_c (block scan), Z = the total;
 //   F. one thread per point: T = t Z, i = min{ j : W_j > T } by chunk -> key;
-//   G. each warp takes S/8 consecutive (sorted) points, loads each distinct V row once
-//      and adds it times its count; out = sum / S.
+//   G. the distinct sampled rows (ordered compaction of the sorted list), each loaded
+//      once -- 16-byte pieces spread over all threads, all in flight -- and added times
+//      its count; out = sum / S.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -42,7 +43,7 @@ __host__ __device__ inline bool gather_xdedup(int G, int S) { return G > 1 && G 
 constexpr int HKCAP = 512;      // heavy keys re-scored per head, at most
 
 struct GatherSmem {
-    int t, O, tot, ce, cm, hot, hv, hvw, hist, idx, acc, qf, all, own, recv, misc, total;
+    int t, O, tot, ce, cm, hot, hv, hvw, hist, idx, lead, acc, qf, all, own, recv, misc, total;
 };
 
 __host__ __device__ inline GatherSmem gather_smem(int D, int G, int S, int nch_used, int mode, bool xd)
@@ -61,7 +62,8 @@ __host__ __device__ inline GatherSmem gather_smem(int D, int G, int S, int nch_u
     s.hvw = off; off = (int)align_up((size_t)off + HKCAP * 4, 16);
     s.hist = off; off = (int)align_up((size_t)off + HBINS * 4, 16);
     s.idx = off; off = (int)align_up((size_t)off + Sp * 4, 16);
-    s.acc = off; off += NWARP * D * 4;
+    s.lead = off; off = (int)align_up((size_t)off + (S + 1) * 4, 16);
+    s.acc = off; off += NT * 8 * 4;  // per-thread partial sums of the gather (8 dims each)
     s.qf = off; off += D * 4;
     s.all = off; off = (int)align_up((size_t)off + (xd ? G * S * 4 : 0), 16);   // the group's G lists
     s.own = off; off = (int)align_up((size_t)off + (xd ? NWARP * G * D * 4 : 0), 16);  // partial sums
@@ -457,62 +459,60 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
             return;
         }
     }
-    const int per = (S + NWARP - 1) / NWARP;
-    const int s0 = min(warp * per, S), s1 = min(s0 + per, S);
-    float acc[EPL];
+    // distinct rows of this head's sorted list (first occurrences, in order) ...
+    int *lead = reinterpret_cast<int *>(smem + lay.lead);
+    {
+        const int per = (S + NT - 1) / NT;
+        const int s0 = min(tid * per, S), s1 = min(s0 + per, S);
+        int cnt = 0;
+        for (int s = s0; s < s1; ++s) cnt += (s == 0 || idx[s] != idx[s - 1]) ? 1 : 0;
+        int nlead;
+        int pos = block_excl_scan(cnt, misc, &nlead);
+        for (int s = s0; s < s1; ++s)
+            if (s == 0 || idx[s] != idx[s - 1]) lead[pos++] = s;
+        if (tid == 0) lead[nlead] = S;
+        __syncthreads();
+        // ... then each thread loads 16-byte pieces (8 dimensions) of every RSTEP-th
+        // distinct row, eight loads in flight, and adds them times their counts; the
+        // RSTEP partial sums of each piece are added in a fixed order
+        constexpr int NPC = D * 2 / 16;   // 16-byte pieces per row
+        constexpr int RSTEP = NT / NPC;   // rows in parallel
+        const int piece = tid % NPC, r0 = tid / NPC;
+        float acc[8];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-    for (int base = s0; base < s1; base += 32) {
-        const int s = base + lane;
-        const bool in = s < s1;
-        const int j = in ? idx[s] : 0;
-        // a run starts at each new index and at the first lane of every batch of 32
-        const bool starts = in && (lane == 0 || idx[s - 1] != j);
-        unsigned lead = __ballot_sync(FULL, starts);
-        const unsigned after = lane == 31 ? 0u : (lead & (~0u << (lane + 1)));
-        const int run = (after ? __ffs(after) - 1 : min(32, s1 - base)) - lane;
-        while (lead) {  // (lead is warp-uniform)
-            constexpr int U = 8;
-            int js[U];
-            float cf[U];
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int l0 = r0; l0 < nlead; l0 += 8 * RSTEP) {
+            uint4 raw[8];
+            float cf[8];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int src = lead ? __ffs(lead) - 1 : 0;
-                const int jv = __shfl_sync(FULL, j, src);
-                const int rn = __shfl_sync(FULL, run, src);
-                js[u] = lead ? jv : 0;
-                cf[u] = lead ? (float)rn : 0.f;
-                lead &= lead - 1u;
-            }
-            float vv[U][EPL];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if constexpr (EPL == 4) {
-                    const uint2 raw = *reinterpret_cast<const uint2 *>(vg + (size_t)js[u] * D + 4 * lane);
-                    vv[u][0] = bf16lo_to_f32(raw.x);
-                    vv[u][1] = bf16hi_to_f32(raw.x);
-                    vv[u][2] = bf16lo_to_f32(raw.y);
-                    vv[u][3] = bf16hi_to_f32(raw.y);
-                } else {
-                    const uint32_t raw = *reinterpret_cast<const uint32_t *>(vg + (size_t)js[u] * D + 2 * lane);
-                    vv[u][0] = bf16lo_to_f32(raw);
-                    vv[u][1] = bf16hi_to_f32(raw);
+            for (int u = 0; u < 8; ++u) {
+                const int li = l0 + u * RSTEP;
+                cf[u] = 0.f;
+                raw[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (li < nlead) {
+                    const int s = lead[li];
+                    cf[u] = (float)(lead[li + 1] - s);
+                    raw[u] = *reinterpret_cast<const uint4 *>(vg + (size_t)idx[s] * D + 8 * piece);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u)
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[e] = __fmaf_rn(cf[u], vv[u][e], acc[e]);
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = __fmaf_rn(cf[u], bf16lo_to_f32(wv[i]), acc[2 * i]);
+                    acc[2 * i + 1] = __fmaf_rn(cf[u], bf16hi_to_f32(wv[i]), acc[2 * i + 1]);
+                }
+            }
         }
-    }
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) acc_s[warp * D + EPL * lane + e] = acc[e];
-    __syncthreads();
-    for (int i = tid; i < D; i += NT) {
-        float sum = 0.f;
-#pragma unroll
-        for (int w = 0; w < NWARP; ++w) sum = __fadd_rn(sum, acc_s[w * D + i]);
-        p.out[(size_t)bh * D + i] = __fdiv_rn(sum, (float)S);
+        for (int e = 0; e < 8; ++e) acc_s[(r0 * NPC + piece) * 8 + e] = acc[e];
+        __syncthreads();
+        for (int i = tid; i < D; i += NT) {
+            float sum = 0.f;
+            for (int r = 0; r < RSTEP; ++r) sum = __fadd_rn(sum, acc_s[(r * NPC + i / 8) * 8 + i % 8]);
+            p.out[(size_t)bh * D + i] = __fdiv_rn(sum, (float)S);
+        }
     }
 }
 
