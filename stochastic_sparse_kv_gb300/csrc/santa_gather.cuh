@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
         float *tot_s = reinterpret_cast<float *>(smem + lay.tot);
         int *ce_s = reinterpret_cast<int *>(smem + lay.ce);
         float *cm_s = reinterpret_cast<float *>(smem + lay.cm);
+#pragma unroll 4
         for (int c = tid; c < nchn; c += NT) {
             const float t = __ldcg(p.ctot + bhc + c);
             const int e = __ldcg(p.cexp + bhc + c);
@@ -242,18 +243,32 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
         __syncthreads();
     }
 
-    // ---- C. heavy keys of the hot chunks: slot q = hot entry * 32 + key
+    // ---- C. heavy keys of the hot chunks: slot q = hot entry * 32 + key; eight loads in
+    // flight per thread before any of them is acted on
     float *wrow = p.w + (size_t)bh * p.n_pad;
-    for (int q = tid; q < nhot * CHUNK; q += NT) {
-        const int c = hot[q / CHUNK];
-        const int j = c * CHUNK + (q % CHUNK);
-        if (j < n) {
-            const float wv = __ldcg(wrow + j);
-            if (wv >= exp2f(thr - (float)cexp[c])) {
+    for (int q0 = tid; q0 < nhot * CHUNK; q0 += 8 * NT) {
+        float wv[8];
+        int jj[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int q = q0 + u * NT;
+            jj[u] = -1;
+            wv[u] = 0.f;
+            if (q < nhot * CHUNK) {
+                const int j = hot[q / CHUNK] * CHUNK + (q % CHUNK);
+                if (j < n) {
+                    jj[u] = j;
+                    wv[u] = __ldcg(wrow + j);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (jj[u] >= 0 && wv[u] >= exp2f(thr - (float)cexp[jj[u] / CHUNK])) {
                 const int pos = atomicAdd(misc + GM_NHV, 1);
                 if (pos < HKCAP) {
-                    hv[pos] = j;
-                    hvw[pos] = wv;
+                    hv[pos] = jj[u];
+                    hvw[pos] = wv[u];
                 }
             }
         }
