@@ -165,14 +165,22 @@ def time_steps(fn, steps, warmup, stream, dist=None):
         b.record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
-    total = t0.elapsed_time(t1)
-    if dist is not None:
-        t = torch.tensor([total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total = float(t.item())
-        dist.barrier()
+    total = max_over_ranks(t0.elapsed_time(t1), dist, "cuda")
     torch.cuda.synchronize()
     return total, [a.elapsed_time(b) for a, b in evs]
+
+
+def max_over_ranks(value, dist=None, device="cpu"):
+    """The largest `value` over all ranks (each rank runs an independent replica; the
+    step takes as long as the slowest), followed by a barrier.  `dist` is
+    torch.distributed or None (one process)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
 
 
 def run_ours(args):
