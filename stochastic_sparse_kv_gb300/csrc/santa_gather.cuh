@@ -14,8 +14,8 @@
 //      G_c = round(tot_c 2^(FIX_F + c_t - C)); hot chunks: maximum >= M - tau2 (at most
 //      HCAP: when more qualify, a histogram of the maxima keeps the hottest);
 //   C. heavy keys: keys of hot chunks whose score is >= M - tau2 (read off their weights);
-//   D. one thread per heavy key re-scores it error-free, rewrites its weight and adds the
-//      fixed-point change to its chunk's G_c (integer atomics: exact, in any order).  The
+//   D. four lanes per heavy key re-score it error-free; its weight is rewritten and the
+//      fixed-point change added to its chunk's G_c (integer atomics: exact, in any order).  The
 //      heaviest keys' fp32 dot-product rounding would otherwise shift every later CDF
 //      boundary;
 //   E. the exact exclusive prefix O_c of the G_c (block scan), Z = the total;
@@ -32,7 +32,7 @@
 namespace santa {
 
 constexpr int NCH_SMEM = 4096;  // a head's chunk arrays stay in shared memory up to this many chunks
-constexpr int HCAP = 128;       // hot chunks re-scored per head, at most
+constexpr int HCAP = 192;       // hot chunks re-scored per head, at most
 constexpr int HBINS = 256;      // histogram bins that pick the hottest HCAP chunks
 constexpr int XDEDUP_MAX = 8192;  // G * S up to which the group's heads share their V loads
 
@@ -276,19 +276,22 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
     __syncthreads();
     const int nhv = min(misc[GM_NHV], HKCAP);
 
-    // ---- D. re-score the heavy keys (one thread each) and patch their chunk totals
+    // ---- D. re-score the heavy keys (four lanes each) and patch their chunk totals
     const uint16_t *kg = p.k + ((size_t)b * p.H_kv + g) * (size_t)p.n_max * D;
-    for (int i = tid; i < nhv; i += NT) {
-        const int j = hv[i];
-        const int c = j / CHUNK;
-        const int ct = cexp[c];
+    for (int i0 = 0; i0 < nhv; i0 += NT / 4) {  // (every lane runs every pass: they shuffle)
+        const int i = i0 + tid / 4, part = tid & 3;
+        const int j = i < nhv ? hv[i] : 0;
         float shi, slo;
-        rescore_key<D>(kg + (size_t)j * D, qf, p.k2_hi, p.k2_lo, shi, slo);
-        const float wnew = exp2f(__fadd_rn(__fsub_rn(shi, (float)ct), slo));
-        wrow[j] = wnew;
-        const int e = FIX_F + ct - Cm;
-        const uint64_t dx = fixp(wnew, e) - fixp(hvw[i], e);  // two's complement difference
-        if (dx) atomicAdd((unsigned long long *)(O + c), (unsigned long long)dx);
+        rescore_key_quad<D>(kg + (size_t)j * D, qf, part, p.k2_hi, p.k2_lo, shi, slo);
+        if (i < nhv && part == 0) {
+            const int c = j / CHUNK;
+            const int ct = cexp[c];
+            const float wnew = exp2f(__fadd_rn(__fsub_rn(shi, (float)ct), slo));
+            wrow[j] = wnew;
+            const int e = FIX_F + ct - Cm;
+            const uint64_t dx = fixp(wnew, e) - fixp(hvw[i], e);  // two's complement difference
+            if (dx) atomicAdd((unsigned long long *)(O + c), (unsigned long long)dx);
+        }
     }
     __syncthreads();
 

@@ -143,46 +143,51 @@ __device__ __forceinline__ void tile_dots(const uint8_t *tile, int kbase, int su
 }
 
 // Error-free score of one K row (global memory) with query head qf (fp32 copies of the
-// bf16 values, shared memory), by one thread.  Products of two bf16 values are exact in
-// fp32; four interleaved compensated sums (Knuth's TwoSum, errors accumulated apart)
-// keep the dependency chains short, and are merged the same way.  Returns the score in
-// log2 units, s * scale * log2(e), as a normalised pair (hi, lo) accurate to about
-// 2^-44 relative.
+// bf16 values, shared memory), by the four lanes of a quad (part = lane & 3: elements
+// [D/4 part, D/4 (part+1))).  Products of two bf16 values are exact in fp32; two
+// interleaved compensated sums per lane (Knuth's TwoSum, errors accumulated apart), then
+// a TwoSum butterfly over the quad.  Every lane of the quad returns the score in log2
+// units, s * scale * log2(e), as a normalised pair (hi, lo) accurate to about 2^-44
+// relative.  All 32 lanes of the warp must call it (it shuffles).
 template <int D>
-__device__ __forceinline__ void rescore_key(const uint16_t *krow, const float *qf, float k2_hi, float k2_lo,
-                                            float &hi, float &lo)
+__device__ __forceinline__ void rescore_key_quad(const uint16_t *krow, const float *qf, int part, float k2_hi,
+                                                 float k2_lo, float &hi, float &lo)
 {
-    float s[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint4 *k4 = reinterpret_cast<const uint4 *>(krow);
+    constexpr int NE = D / 4;  // elements per lane: 32 or 16
+    const uint4 *k4 = reinterpret_cast<const uint4 *>(krow + NE * part);
+    const float *qp = qf + NE * part;
+    uint4 kv[NE / 8];
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {  // 16-byte chunks of 8 elements
-        const uint4 kv = __ldcg(k4 + c);
-        const uint32_t wv[4] = {kv.x, kv.y, kv.z, kv.w};
+    for (int c = 0; c < NE / 8; ++c) kv[c] = __ldcg(k4 + c);
+    float s0 = 0.f, e0 = 0.f, s1 = 0.f, e1 = 0.f, t;
+#pragma unroll
+    for (int c = 0; c < NE / 8; ++c) {
+        const uint32_t wv[4] = {kv[c].x, kv[c].y, kv[c].z, kv[c].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int d0 = 8 * c + 2 * i;
-            const int a = (2 * i) & 3, b2 = (2 * i + 1) & 3;
-            float t;
-            two_sum(s[a], __fmul_rn(qf[d0], bf16lo_to_f32(wv[i])), s[a], t);
-            e[a] = __fadd_rn(e[a], t);
-            two_sum(s[b2], __fmul_rn(qf[d0 + 1], bf16hi_to_f32(wv[i])), s[b2], t);
-            e[b2] = __fadd_rn(e[b2], t);
+            two_sum(s0, __fmul_rn(qp[d0], bf16lo_to_f32(wv[i])), s0, t);
+            e0 = __fadd_rn(e0, t);
+            two_sum(s1, __fmul_rn(qp[d0 + 1], bf16hi_to_f32(wv[i])), s1, t);
+            e1 = __fadd_rn(e1, t);
         }
     }
-    float S0, E0, S1, E1, t;
-    two_sum(s[0], s[1], S0, t);
-    E0 = __fadd_rn(__fadd_rn(e[0], e[1]), t);
-    two_sum(s[2], s[3], S1, t);
-    E1 = __fadd_rn(__fadd_rn(e[2], e[3]), t);
-    float sum, err;
-    two_sum(S0, S1, sum, t);
-    err = __fadd_rn(__fadd_rn(E0, E1), t);
-    fast_two_sum(sum, err, sum, err);
-    // (sum + err) * (k2_hi + k2_lo) to about 2^-46 relative
-    const float P = __fmul_rn(sum, k2_hi);
-    float E = __fmaf_rn(sum, k2_hi, -P);
-    E = __fmaf_rn(sum, k2_lo, E);
-    E = __fmaf_rn(err, k2_hi, E);
+    float s, e;
+    two_sum(s0, s1, s, t);
+    e = __fadd_rn(__fadd_rn(e0, e1), t);
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, m);
+        const float e2 = __shfl_xor_sync(0xffffffffu, e, m);
+        two_sum(s, s2, s, t);
+        e = __fadd_rn(__fadd_rn(e, e2), t);
+    }
+    fast_two_sum(s, e, s, e);
+    // (s + e) * (k2_hi + k2_lo) to about 2^-46 relative
+    const float P = __fmul_rn(s, k2_hi);
+    float E = __fmaf_rn(s, k2_hi, -P);
+    E = __fmaf_rn(s, k2_lo, E);
+    E = __fmaf_rn(e, k2_hi, E);
     fast_two_sum(P, E, hi, lo);
 }
 
