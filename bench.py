@@ -30,7 +30,7 @@ UNIT = "us/step"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "santa_decode_b16_32k_traffic.txt")
 CSRC = os.path.join("stochastic_sparse_kv_gb300", "csrc")
-KERNEL_SOURCES = [os.path.join(CSRC, f) for f in ("santa_common.cuh", "santa_sample.cuh", "santa_score.cuh",
+KERNEL_SOURCES = [os.path.join(CSRC, f) for f in ("santa_common.cuh", "santa_sample.cuh", "santa_tcgen05.cuh", "santa_score.cuh",
                                                    "santa_gather.cuh", "santa_dense.cuh", "santa_api.cu")]
 # The sampled path is two launches chained by programmatic dependent launch (the value
 # stage overlaps the score kernel's tail), so one santa_decode call is timed as the unit.

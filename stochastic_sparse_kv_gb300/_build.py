@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsanta.so")
 UNITS = ["santa_api.cu", "santa_kernels_d128.cu", "santa_kernels_d64.cu"]
-HEADERS = ["santa_common.cuh", "santa_sample.cuh", "santa_score.cuh", "santa_gather.cuh", "santa_dense.cuh",
+HEADERS = ["santa_common.cuh", "santa_sample.cuh", "santa_tcgen05.cuh", "santa_score.cuh", "santa_gather.cuh", "santa_dense.cuh",
            "santa_kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -15,7 +15,8 @@ namespace santa {
 
 int score_smem_bytes(int D, int G, int B)
 {
-    return score_smem(D, G, B).total;
+    (void)G;
+    return score_smem(D, B).total;
 }
 
 int gather_smem_bytes(int D, int G, int S, int nch_used, int mode, bool xdedup)
@@ -119,7 +120,7 @@ int device_info(int *dev, int *sms, int *optin)
 }
 
 // Raise the kernel's dynamic shared-memory limit if needed; return CTAs per SM.
-int prepare_fn(const void *fn, int dev, int smem, int *occ)
+int prepare_fn(const void *fn, int dev, int smem, int threads, int *occ)
 {
     std::lock_guard<std::mutex> lk(g_mu);
     FnCache *c = nullptr;
@@ -141,7 +142,7 @@ int prepare_fn(const void *fn, int dev, int smem, int *occ)
     }
     if (c->occ_smem != smem) {
         int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, fn, NT, smem) != cudaSuccess) return SANTA_ERR_CUDA;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, fn, threads, smem) != cudaSuccess) return SANTA_ERR_CUDA;
         c->occ = o;
         c->occ_smem = smem;
     }
@@ -174,16 +175,41 @@ int check_mode_S(int32_t mode_flags, int32_t S)
     return SANTA_OK;
 }
 
-// Keys per work unit of the sampled path's score kernel: 128, or 64 or 32 when the
-// problem has too few 128-key units to keep every warp (NWARP per SM) busy to the end.
-int choose_unit_sampled(const santa_shape *sh, int sms)
+// cuTensorMapEncodeTiled from the driver, found once through the runtime (no link
+// against libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled()
 {
-    const long long warps = (long long)sms * NWARP;
-    for (int L = UNIT_KEYS; L > CHUNK; L /= 2) {
-        const long long units = (long long)sh->B * sh->H_kv * ((sh->n_max + L - 1) / L);
-        if (units >= 4 * warps) return L;
-    }
-    return CHUNK;
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult qr{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix [rows][D] as a 2-D tensor map with boxes of 64 columns (128
+// bytes, the 128-byte swizzle's width) by box_rows rows.
+int make_map_bf16(CUtensorMap *map, const void *base, int D, long long rows, int box_rows)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return SANTA_ERR_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SANTA_OK : SANTA_ERR_CUDA;
 }
 
 }  // namespace
@@ -257,7 +283,9 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     int dev, sms, optin;
     if ((rc = device_info(&dev, &sms, &optin))) return rc;
     const int D = shape->d, G = shape->H_q / shape->H_kv;
-    const int L = dense ? DENSE_UNIT : choose_unit_sampled(shape, sms);  // keys per work unit
+    const int L = dense ? DENSE_UNIT : SC_M;  // keys per work unit
+    // the score kernel addresses K rows with 32-bit TMA coordinates
+    if (!dense && (long long)shape->B * shape->H_kv * shape->n_max >= (1ll << 31)) return SANTA_ERR_UNSUPPORTED;
 
     Params p{};
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -302,8 +330,9 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     if (!fn) return SANTA_ERR_UNSUPPORTED;
     const int smem = dense ? dense_smem_bytes(D, G, shape->B) : score_smem_bytes(D, G, shape->B);
     if (smem > optin) return SANTA_ERR_UNSUPPORTED;
+    const int threads = dense ? NT : SC_NT;
     int occ = 0;
-    if ((rc = prepare_fn(fn, dev, smem, &occ))) return rc;
+    if ((rc = prepare_fn(fn, dev, smem, threads, &occ))) return rc;
     const void *fn2 = nullptr;
     int smem2 = 0;
     if (!dense) {
@@ -312,16 +341,30 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
         smem2 = gather_smem_bytes(D, G, p.S, p.nch, mode, p.xdedup != 0);
         if (smem2 > optin) return SANTA_ERR_UNSUPPORTED;
         int occ2 = 0;
-        if ((rc = prepare_fn(fn2, dev, smem2, &occ2))) return rc;
+        if ((rc = prepare_fn(fn2, dev, smem2, NT, &occ2))) return rc;
     }
     const long long items = (long long)shape->B * shape->H_kv * ((shape->n_max + L - 1) / L);
     long long grid = (long long)sms * occ;
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;
     void *args[] = {&p};
-    if (cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(NT), args, (size_t)smem, (cudaStream_t)stream) !=
-        cudaSuccess)
-        return SANTA_ERR_CUDA;
+    if (dense) {
+        if (cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(NT), args, (size_t)smem, (cudaStream_t)stream) !=
+            cudaSuccess)
+            return SANTA_ERR_CUDA;
+    } else {
+        // K as [B*H_kv*n_max][d] in boxes of a whole unit (SC_M rows) and of SC_BOX_ROWS rows
+        // (a sequence's last unit); q as [B*H_q][d] in boxes of one group's G heads
+        CUtensorMap tm_k, tm_kt, tm_q;
+        const long long krows = (long long)shape->B * shape->H_kv * shape->n_max;
+        if ((rc = make_map_bf16(&tm_k, k_cache, D, krows, SC_M))) return rc;
+        if ((rc = make_map_bf16(&tm_kt, k_cache, D, krows, SC_BOX_ROWS))) return rc;
+        if ((rc = make_map_bf16(&tm_q, q, D, (long long)shape->B * shape->H_q, G))) return rc;
+        void *sargs[] = {&p, &tm_k, &tm_kt, &tm_q};
+        if (cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(SC_NT), sargs, (size_t)smem, (cudaStream_t)stream) !=
+            cudaSuccess)
+            return SANTA_ERR_CUDA;
+    }
     if (!dense) {
         // value stage: one CTA per (b, h_q), a programmatic dependent of the score kernel;
         // the G heads of a group form a cluster when they share V loads

@@ -16,7 +16,6 @@ namespace santa {
 
 constexpr int NT = 256;              // threads per CTA
 constexpr int NWARP = NT / 32;       // 8 warps
-constexpr int UNIT_KEYS = 128;       // keys per work unit of the sampled score kernel (at most)
 constexpr int LMIN = 128;            // (tile-size check of the score helpers)
 constexpr int DENSE_UNIT = 512;      // keys per work unit (and per partial) of the dense kernel
 constexpr int CHUNK = 32;            // keys per CDF chunk (one 128-byte line of fp32 w)

@@ -2,20 +2,23 @@
 //
 // "Stochastic Sparse Attention for Memory-Bound Inference" (abstract): the score stage
 // reads all n_k cached keys and forms the post-softmax distribution from which the
-// value stage samples.  This is the kernel that streams the K cache (about 97% of the
-// bytes of a sampled decode step), so it is built for bandwidth:
+// value stage samples.  This kernel streams the K cache (about 97% of the bytes of a
+// sampled decode step) and is built so that nothing but that stream limits it:
 //
-//  * persistent CTAs of 8 independent warps; a warp takes work units of L consecutive
-//    keys of one KV head g of one batch row b -- a static contiguous block of units
-//    first, then grabs from a global counter that shrink to single units near the end,
-//    so that the warps finish together -- and streams them through its own ring of 32-key tiles, filled by 1-D TMA bulk copies (cp.async.bulk, completion
-//    on an mbarrier) that lane 0 issues; K is read with an L2 evict-first hint, and the
-//    weights and chunk data are written with evict-last, for the value stage;
-//  * the group's query heads ride along with the first tile of a new (b, g) as a second
-//    bulk copy on the same barrier, so a warp does not stall on a query load;
-//  * no CTA-wide barrier after the prologue: a warp waits only for its own tiles;
-//  * one tile is one CDF chunk of 32 keys with its own power-of-two scale, so chunks
-//    are independent: nothing is carried from one tile to the next.
+//  * the contraction q . K^T runs on the tensor cores (tcgen05, bf16 inputs, fp32
+//    accumulation in TMEM): a work unit is 128 consecutive keys of one KV head g of one
+//    batch row b, and one unit is an M=128 x N=16 x K=d product whose N columns are the
+//    group's G query heads (the rest padding).  The SIMT units keep only the softmax
+//    epilogue (a handful of instructions per key instead of d*G/2 packed FMAs);
+//  * persistent CTAs, one per SM, warp-specialised: one thread streams K tiles with
+//    tiled TMA copies (128-byte swizzle, L2 evict-first) into a ring of stages, one
+//    thread issues the MMAs, and two warpgroups of epilogue warps turn accumulators
+//    into weights; mbarriers link the three (every wait bounded);
+//  * a static contiguous block of units per CTA (about 80% of the work), then grabs
+//    from a global counter that shrink from four units to one near the end, requested
+//    one grab ahead;
+//  * one epilogue warp handles one 32-key CDF chunk (its TMEM lane quarter), so chunks
+//    are independent and need no state across units.
 //
 // Per query head of the group and per chunk it leaves in the workspace:
 //   w_j    fp32 weight 2^(s_j log2 e - c_t), c_t = ceil(the chunk's maximum of s log2 e),
@@ -33,303 +36,414 @@
 #pragma once
 
 #include "santa_sample.cuh"
+#include "santa_tcgen05.cuh"
 
 namespace santa {
 
-template <int D, int G>
-struct ScoreTile {
-    static constexpr int KEYS = CHUNK;                   // keys per warp tile = one CDF chunk
-    static constexpr int BYTES = KEYS * 2 * D;           // 8 KB at d=128, 4 KB at d=64
-    static constexpr int NSTAGE = 24576 / BYTES;         // 24 KB of ring per warp
-    static constexpr int QBYTES = G * D * 2;             // the group's query heads, bf16
-    static constexpr int QBUF = QBYTES <= 1024 ? 2 : 1;  // staging buffers for them
-};
+constexpr int SC_M = 128;              // keys per work unit = MMA rows
+constexpr int SC_N = 16;               // MMA columns (query heads of the group, padded)
+constexpr int SC_CHAIN = 1;            // K=16 MMA steps accumulated into one TMEM partial
+constexpr int SC_TMEM_COLS = 512;      // all of TMEM: accumulators of every unit in flight
+constexpr int SC_EPI_WARPS = 8;        // two warpgroups
+constexpr int SC_WARP_PROD = 8;        // TMA producer
+constexpr int SC_WARP_MMA = 9;         // MMA issuer, owner of the TMEM allocation
+constexpr int SC_NT = 320;             // threads per CTA
+constexpr int SC_BOX_ROWS = 32;        // rows per TMA box of a unit's tail (one CDF chunk)
+constexpr int SC_RING_BYTES = 221184;  // stage ring (K + query tiles)
+
+__host__ __device__ constexpr int score_halves(int D) { return D / 64; }  // 128-byte column blocks of a row
+__host__ __device__ constexpr int score_kbytes(int D) { return score_halves(D) * SC_M * 128; }
+__host__ __device__ constexpr int score_qbytes(int D) { return score_halves(D) * SC_N * 128; }
+__host__ __device__ constexpr int score_stages(int D) { return SC_RING_BYTES / (score_kbytes(D) + score_qbytes(D)); }
+// A unit's scores are the fp32 sum of D/(16*SC_CHAIN) partials, each SC_N TMEM columns;
+// accumulators (units in flight between the MMA and the epilogue) fill the TMEM.
+__host__ __device__ constexpr int score_chain(int D) { return SC_CHAIN < D / 16 ? SC_CHAIN : D / 16; }
+__host__ __device__ constexpr int score_parts(int D) { return D / 16 / score_chain(D); }
+__host__ __device__ constexpr int score_ucols(int D) { return score_parts(D) * SC_N; }
+__host__ __device__ constexpr int score_nacc(int D)
+{
+    return SC_TMEM_COLS / score_ucols(D) < 32 ? SC_TMEM_COLS / score_ucols(D) : 32;
+}
 
 struct ScoreSmem {
-    int nb, prefix, misc, warp0, warp_bytes, ring, qbuf, bar, desc, total;
+    int kst, qst, bar, desc, adesc, tmem, nb, prefix, total;
 };
 
-__host__ __device__ inline ScoreSmem score_smem(int D, int G, int B)
+// Byte offsets from the 1024-aligned base; `total` includes the alignment slack.
+__host__ __device__ inline ScoreSmem score_smem(int D, int B)
 {
-    const int bytes = CHUNK * 2 * D;
-    const int nstage = 24576 / bytes;
-    const int qbytes = G * D * 2;
-    const int qbuf = qbytes <= 1024 ? 2 : 1;
+    const int ns = score_stages(D), nacc = score_nacc(D);
     ScoreSmem s{};
     int off = 0;
+    s.kst = off; off += ns * score_kbytes(D);
+    s.qst = off; off += ns * score_qbytes(D);
+    s.bar = off; off += (int)align_up((size_t)(2 * ns + 2 * nacc + 1) * 8, 16);
+    s.desc = off; off += ns * 16;
+    s.adesc = off; off += nacc * 16;
+    s.tmem = off; off += 16;
     s.nb = off; off += (int)align_up((size_t)B * 4, 16);
     s.prefix = off; off += (int)align_up((size_t)(B + 1) * 4, 16);
-    s.misc = off; off += 16 * 4;
-    s.warp0 = (int)align_up((size_t)off, 128);
-    // per-warp block (offsets relative to the warp's base)
-    int w = 0;
-    s.ring = w; w += nstage * bytes;
-    s.qbuf = w; w += qbuf * qbytes;
-    s.bar = w; w += nstage * 8;
-    s.desc = w = (int)align_up((size_t)w, 16); w += nstage * 16;
-    s.warp_bytes = (int)align_up((size_t)w, 128);
-    s.total = s.warp0 + NWARP * s.warp_bytes;
+    s.total = off + 1024;
     return s;
 }
 
+// The work-item space of the sampled path, built by one warp: nb[b] (checked lengths)
+// and prefix[0..B] of the unit counts H_kv * ceil(n_b / SC_M) (H_kv for n_b = 0).
+__device__ __forceinline__ void score_item_space(const Params &p, int *nb, int *prefix)
+{
+    constexpr int PER = BMAX / 32;
+    const int lane = threadIdx.x & 31;
+    int sum = 0;
+    bool bad = false;
+#pragma unroll 8
+    for (int i = 0; i < PER; ++i) {
+        const int b = lane * PER + i;
+        if (b < p.B) {
+            int n = p.seq_lens[b];
+            if (n < 0 || n > p.n_max) {
+                bad = true;
+                n = 0;
+            }
+            nb[b] = n;
+            sum += p.H_kv * (n > 0 ? (n + SC_M - 1) / SC_M : 1);
+        }
+    }
+    int x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    int run = x - sum;
+    for (int i = 0; i < PER; ++i) {
+        const int b = lane * PER + i;
+        if (b < p.B) {
+            prefix[b] = run;
+            run += p.H_kv * (nb[b] > 0 ? (nb[b] + SC_M - 1) / SC_M : 1);
+        }
+    }
+    if (lane == 31) prefix[p.B] = x;
+    if (bad && blockIdx.x == 0) set_dev_error(p.ctrl, DEV_BAD_SEQLEN);
+    __syncwarp();
+}
 
 template <int D, int G>
-__global__ void __launch_bounds__(NT, 1) santa_score_kernel(const Params p)
+__global__ void __launch_bounds__(SC_NT, 1)
+    santa_score_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_kt,
+                       const __grid_constant__ CUtensorMap tm_q)
 {
-    using C = SampleCfg<D, G>;
-    using T = ScoreTile<D, G>;
-    constexpr int NSTAGE = T::NSTAGE;
-    constexpr int NCALL = T::KEYS / C::KW;  // tile_dots calls per tile
-    constexpr int NV = C::NV;
+    constexpr int NH = score_halves(D);
+    constexpr int KB = SC_M * 128;   // one 128-byte column block of a K tile: 16 KB
+    constexpr int QB = SC_N * 128;   // one column block of the query tile: 2 KB
+    constexpr int NS = score_stages(D);
+    constexpr int CH = score_chain(D);      // MMA steps per partial
+    constexpr int NP = score_parts(D);      // partial sums per score
+    constexpr int UCOLS = score_ucols(D);   // TMEM columns per unit
+    constexpr int NACC = score_nacc(D);     // accumulators: unit j uses j % NACC
+    static_assert(NACC >= 2 && NACC % 2 == 0 && NACC * UCOLS <= SC_TMEM_COLS, "TMEM accumulators");
+    constexpr uint32_t IDESC = idesc_bf16_f32(SC_M, SC_N);
     constexpr unsigned FULL = 0xffffffffu;
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int sub = lane % C::P, grp = lane / C::P;
-    const int B = p.B, H_kv = p.H_kv, L = p.L;  // L: keys per work unit
-    const ScoreSmem lay = score_smem(D, G, B);
+    static_assert(G >= 1 && G <= 8 && SC_N >= G, "query heads per group");
+    static_assert(NS >= 2, "stage ring");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const int B = p.B, H_kv = p.H_kv;
+    const ScoreSmem lay = score_smem(D, B);
+    uint8_t *kst = smem + lay.kst;
+    uint8_t *qst = smem + lay.qst;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar);
+    uint64_t *empty = full + NS;
+    uint64_t *tfull = empty + NS;
+    uint64_t *tempty = tfull + NACC;
+    uint64_t *drain = tempty + NACC;
+    int4 *desc = reinterpret_cast<int4 *>(smem + lay.desc);
+    int4 *adesc = reinterpret_cast<int4 *>(smem + lay.adesc);
+    // [0] the TMEM address, [1] full phases the MMA thread consumed, [2] stages filled
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + lay.tmem);
     int *nb = reinterpret_cast<int *>(smem + lay.nb);
     int *prefix = reinterpret_cast<int *>(smem + lay.prefix);
-    int *misc = reinterpret_cast<int *>(smem + lay.misc);
-    uint8_t *wb = smem + lay.warp0 + warp * lay.warp_bytes;
-    uint8_t *ring = wb + lay.ring;
-    uint8_t *qbuf = wb + lay.qbuf;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(wb + lay.bar);
-    int4 *desc = reinterpret_cast<int4 *>(wb + lay.desc);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float NEG_INF = __int_as_float(0xff800000);
 
-    build_item_space(p, nb, prefix, misc);
-    if (lane == 0) {
-        for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
-        mbar_fence_init();
+    // ---- setup: TMEM, barriers, the work-item space, zero padding rows of the query tiles
+    if (warp == SC_WARP_MMA) {
+        tmem_alloc(tmem_slot, SC_TMEM_COLS);
+        tmem_relinquish();
     }
-    __syncthreads();  // the only CTA-wide barrier of the main path
-    const int total_items = prefix[B];
-    // Work schedule: about 80% of the units as one contiguous static block per warp (no
-    // atomics, long sequential streams); the rest handed out from a global counter in
-    // grabs that shrink from four units to one as the work runs out, so that the warps
-    // finish together.  Each grab is requested one grab ahead, so its atomic never
-    // stalls the warp.
-    const int W = (int)gridDim.x * NWARP;
-    const int gw = (int)blockIdx.x * NWARP + warp;
-    const int Ks = (int)((long long)total_items * 4 / 5 / W);  // static units per warp
-    const int dyn0 = Ks * W;                                    // the first dynamic unit
-
-    // ---- producer state (warp-uniform; lane 0 issues the copies and the atomics)
-    uint64_t policy = 0;
-    const uint64_t keep = l2_policy_evict_last();  // the value stage reads these back
-    int pend = 0;  // lane 0: the outstanding grab, first unit * 8 + size
-    auto request = [&](int last) {
+    if (warp == SC_WARP_PROD) {
         if (lane == 0) {
-            const int k = max(1, min(4, (total_items - last) / (2 * W)));
-            pend = (dyn0 + atomicAdd(p.ctrl + CTRL_WORK, k)) * 8 + k;
-        }
-    };
-    if (lane == 0) policy = l2_policy_evict_first();
-    request(dyn0);
-    int g_next = gw * Ks, g_end = g_next + Ks;  // the current grab: the static block first
-    int pr_r = 0, pr_tile = 0, pr_ntiles = 0, pr_valid = 0, pr_grp = 0;
-    long long pr_row0 = 0;
-    bool pr_end = false;
-    int pr_group = -1;          // (b * H_kv + g) of the last unit issued
-    int q_issue0 = -1, q_issue1 = -1;  // sequence number of the tile carrying each q buffer
-    int q_next = 0;             // the q buffer to use next
-    int pr_seq = 0;             // sequence number of the next tile issued
-    // position (b, g, r) of unit g_next, found by one search per grab and then stepped
-    int ub = 0, ug = 0, ur = 0, uns = 1;
-    auto seek = [&](int itm) {
-        const Item x = decode_item(itm, prefix, nb, B, H_kv, L);
-        ub = x.b;
-        ug = x.g;
-        ur = x.r;
-        uns = x.ns;
-    };
-    auto step = [&]() {
-        if (++ur == uns) {
-            ur = 0;
-            if (++ug == H_kv) {
-                ug = 0;
-                if (++ub < B) uns = nb[ub] > 0 ? (nb[ub] + L - 1) / L : 1;
+            tmem_slot[1] = 0;
+            tmem_slot[2] = 0;
+            tma_prefetch_map(&tm_k);
+            tma_prefetch_map(&tm_kt);
+            tma_prefetch_map(&tm_q);
+            for (int s = 0; s < NS; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], 1);
             }
+            for (int a = 0; a < NACC; ++a) {
+                mbar_init(&tfull[a], 2);      // the MMA commit and the issuing thread
+                mbar_init(&tempty[a], 4);     // the four warps of the epilogue warpgroup
+            }
+            mbar_init(drain, 1);
+            mbar_fence_init();
         }
-    };
-    if (g_next < g_end) seek(g_next);
-    auto produce = [&](int slot, int cons_seq) {
-        while (!pr_end && pr_tile == pr_ntiles) {
-            if (g_next == g_end) {
-                const int got = __shfl_sync(FULL, pend, 0);
-                g_next = got >> 3;
-                g_end = min(g_next + (got & 7), total_items);
-                if (g_next >= total_items) {
-                    pr_end = true;
+        score_item_space(p, nb, prefix);
+    }
+    // rows G..SC_N-1 of every query tile: zero (the TMA copies fill rows 0..G-1)
+    {
+        constexpr int PIECES = (SC_N - G) * 8;  // 16-byte pieces per column block
+        for (int i = tid; i < NS * NH * PIECES; i += SC_NT) {
+            const int blk = i / PIECES, rem = i % PIECES;
+            *reinterpret_cast<uint4 *>(qst + blk * QB + (G + rem / 8) * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == SC_WARP_PROD) {
+        // ================= producer: one thread streams K (and the group's queries)
+        if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();
+            const int total_items = prefix[B];
+            const int W = (int)gridDim.x;
+            const int Ks = (int)((long long)total_items * 4 / 5 / W);  // static units per CTA
+            const int dyn0 = Ks * W;
+            auto request = [&](int last) {
+                const int k = max(1, min(4, (total_items - last) / (2 * W)));
+                return (dyn0 + atomicAdd(p.ctrl + CTRL_WORK, k)) * 8 + k;
+            };
+            int pend = request(dyn0);
+            int g_next = (int)blockIdx.x * Ks, g_end = g_next + Ks;
+            int ub = 0, ug = 0, ur = 0, uns = 1;
+            auto seek = [&](int itm) {
+                const Item x = decode_item(itm, prefix, nb, B, H_kv, SC_M);
+                ub = x.b;
+                ug = x.g;
+                ur = x.r;
+                uns = x.ns;
+            };
+            if (g_next < g_end) seek(g_next);
+            int i = 0;
+            for (;; ++i) {
+                // the next unit with keys, or the end of the work
+                int n = 0, b = 0, g = 0, r = 0;
+                bool have = false;
+                while (!have) {
+                    if (g_next == g_end) {
+                        g_next = pend >> 3;
+                        g_end = min(g_next + (pend & 7), total_items);
+                        if (g_next >= total_items) break;
+                        pend = request(g_end);
+                        seek(g_next);
+                    }
+                    n = nb[ub];
+                    b = ub;
+                    g = ug;
+                    r = ur;
+                    ++g_next;
+                    if (++ur == uns) {
+                        ur = 0;
+                        if (++ug == H_kv) {
+                            ug = 0;
+                            if (++ub < B) uns = nb[ub] > 0 ? (nb[ub] + SC_M - 1) / SC_M : 1;
+                        }
+                    }
+                    have = n > 0;  // empty rows are written by the value stage
+                }
+                const int s = i % NS;
+                if (!mbar_wait_bounded(&empty[s], ((uint32_t)(i / NS) & 1u) ^ 1u, p.wait_ns)) {
+                    set_dev_error(p.ctrl, DEV_TIMEOUT);
                     break;
                 }
-                request(g_end);
-                seek(g_next);
-            }
-            const int n = nb[ub];
-            const int b = ub, g = ug, r = ur;
-            ++g_next;
-            step();
-            if (n == 0) continue;  // empty rows are written by the value stage
-            pr_r = r;
-            pr_tile = 0;
-            pr_valid = min(L, n - r * L);
-            pr_ntiles = (pr_valid + T::KEYS - 1) / T::KEYS;
-            pr_grp = b * H_kv + g;
-            pr_row0 = (long long)pr_grp * p.n_max + (long long)r * L;
-        }
-        if (pr_end) {
-            if (lane == 0) desc[slot] = make_int4(DESC_END, 0, 0, 0);
-            return;
-        }
-        const int rows = min(T::KEYS, pr_valid - pr_tile * T::KEYS);
-        int flags = 0;
-        uint32_t qbytes = 0;
-        int qb = 0;
-        if (pr_tile == 0) {
-            if (pr_grp != pr_group) {
-                pr_group = pr_grp;
-                flags |= TF_NEWQ;
-                qb = (T::QBUF == 2) ? q_next : 0;
-                const int busy = qb ? q_issue1 : q_issue0;
-                // a staging buffer is free once the consumer has started the tile that carried it
-                if (busy <= cons_seq) {
-                    if (qb) q_issue1 = pr_seq; else q_issue0 = pr_seq;
-                    if (T::QBUF == 2) q_next ^= 1;
-                    flags |= qb << TF_QB_SHIFT;
-                    qbytes = T::QBYTES;
-                } else {
-                    flags |= TF_QGLOBAL;
+                if (!have) {
+                    desc[s] = make_int4(DESC_END, 0, 0, 0);
+                    mbar_arrive(&full[s]);
+                    ++i;
+                    break;
                 }
+                const int valid = min(SC_M, n - r * SC_M);
+                const int grp = b * H_kv + g;
+                desc[s] = make_int4(grp, r, valid, 0);
+                const int row0 = grp * p.n_max + r * SC_M;
+                uint8_t *kt = kst + s * NH * KB;
+                if (valid == SC_M) {
+                    // a full unit: one 128-row box per 128-byte column block
+                    mbar_arrive_tx(&full[s], (uint32_t)(NH * KB + NH * G * 128));
+#pragma unroll
+                    for (int hf = 0; hf < NH; ++hf) tma_load_2d(kt + hf * KB, &tm_k, hf * 64, row0, &full[s], policy);
+                } else {
+                    // the sequence's last unit: 32-row boxes up to its last key
+                    const int nbox = (valid + SC_BOX_ROWS - 1) / SC_BOX_ROWS;
+                    mbar_arrive_tx(&full[s], (uint32_t)(nbox * NH * SC_BOX_ROWS * 128 + NH * G * 128));
+                    for (int j = 0; j < nbox; ++j)
+#pragma unroll
+                        for (int hf = 0; hf < NH; ++hf)
+                            tma_load_2d(kt + hf * KB + j * SC_BOX_ROWS * 128, &tm_kt, hf * 64, row0 + j * SC_BOX_ROWS,
+                                        &full[s], policy);
+                }
+#pragma unroll
+                for (int hf = 0; hf < NH; ++hf)
+                    tma_load_2d_plain(qst + (s * NH + hf) * QB, &tm_q, hf * 64, grp * G, &full[s]);
             }
+            tmem_slot[2] = (uint32_t)i;
         }
-        if (lane == 0) {
-            desc[slot] = make_int4(pr_grp, (pr_r << 8) | pr_tile, rows, flags);
-            const uint32_t bytes = (uint32_t)rows * C::ROWB;
-            mbar_arrive_tx(&bars[slot], bytes + qbytes);
-            bulk_g2s(ring + slot * T::BYTES, p.k + (pr_row0 + (long long)pr_tile * T::KEYS) * D, bytes,
-                     &bars[slot], policy);
-            // q[b][g*G .. g*G+G-1][:] is contiguous: the group's heads in one copy
-            if (qbytes) bulk_g2s_plain(qbuf + qb * T::QBYTES, p.q + (size_t)pr_grp * G * D, qbytes, &bars[slot]);
-        }
-        ++pr_tile;
-        ++pr_seq;
-    };
-    for (int s = 0; s < NSTAGE; ++s) produce(s, -1);
-
-    // ---- consumer
-    unsigned long long qp[G][8];
-    bool aborted = false;
-    int it = 0;
-    for (;; ++it) {
-        const int slot = it % NSTAGE;
         __syncwarp();
-        const int4 dsc = desc[slot];
-        if (dsc.x == DESC_END) break;
-        if (!mbar_wait_bounded(&bars[slot], (uint32_t)(it / NSTAGE) & 1u, p.wait_ns)) {
-            aborted = true;
-            break;
+    } else if (warp == SC_WARP_MMA) {
+        // ================= MMA issuer: one thread; accumulator a = unit % NACC
+        if (lane == 0) {
+            int j = 0;
+            for (;; ++j) {
+                const int s = j % NS, a = j % NACC;
+                if (!mbar_wait_bounded(&full[s], (uint32_t)(j / NS) & 1u, p.wait_ns)) {
+                    set_dev_error(p.ctrl, DEV_TIMEOUT);
+                    break;
+                }
+                tmem_slot[1] = (uint32_t)(j + 1);
+                const int4 d = desc[s];
+                if (!mbar_wait_bounded(&tempty[a], ((uint32_t)(j / NACC) & 1u) ^ 1u, p.wait_ns)) {
+                    set_dev_error(p.ctrl, DEV_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                adesc[a] = d;
+                if (d.x == DESC_END) {
+                    // both epilogue warpgroups must see the end: units j and j + 1
+                    mbar_arrive(&tfull[a]);
+                    mbar_arrive(&tfull[a]);
+                    const int a1 = (j + 1) % NACC;
+                    if (mbar_wait_bounded(&tempty[a1], ((uint32_t)((j + 1) / NACC) & 1u) ^ 1u, p.wait_ns)) {
+                        adesc[a1] = d;
+                        mbar_arrive(&tfull[a1]);
+                        mbar_arrive(&tfull[a1]);
+                    } else {
+                        set_dev_error(p.ctrl, DEV_TIMEOUT);
+                    }
+                    break;
+                }
+                const uint32_t kaddr = smem_u32(kst + s * NH * KB), qaddr = smem_u32(qst + s * NH * QB);
+                const uint32_t dt = tbase + (uint32_t)(a * UCOLS);
+                // step t = 4*hf + k covers d in [16t, 16t+16); partial t / CH takes CH steps
+#pragma unroll
+                for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int t = 4 * hf + k;
+                        tc_mma_bf16(dt + (uint32_t)((t / CH) * SC_N), umma_desc_sw128(kaddr + hf * KB + k * 32),
+                                    umma_desc_sw128(qaddr + hf * QB + k * 32), IDESC, (t % CH) != 0);
+                    }
+                tc_commit(&empty[s]);   // the stage may be refilled once these MMAs have read it
+                tc_commit(&tfull[a]);   // the accumulator is ready
+                mbar_arrive(&tfull[a]); // (releases adesc[a])
+            }
+            // every MMA complete before the allocation is released
+            tc_commit(drain);
+            mbar_wait_bounded(drain, 0u, p.wait_ns);
         }
-        // descriptor: group b*H_kv + g, (unit r << 8) | tile, rows, flags
-        const int grpid = dsc.x, tile = dsc.y & 0xff, ur_c = dsc.y >> 8, rows = dsc.z, flags = dsc.w;
-        if (flags & TF_NEWQ) {
-            // the group's query heads: fp32 pairs of the lane's two 16-byte chunks per head
-            const uint16_t *qg = (flags & TF_QGLOBAL)
-                                     ? p.q + (size_t)grpid * G * D
-                                     : reinterpret_cast<const uint16_t *>(qbuf + ((flags >> TF_QB_SHIFT) & 1) * T::QBYTES);
+        __syncwarp();
+    } else {
+        // ================= epilogue: warp (e, w4) turns keys 32*w4.. of units e, e+2, ... into weights
+        const int e = warp >> 2, w4 = warp & 3;
+        const uint64_t keep = l2_policy_evict_last();  // the value stage reads these back
+        for (int u = 0;; ++u) {
+            const int j = 2 * u + e, a = j % NACC;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait_bounded(&tfull[a], (uint32_t)(j / NACC) & 1u, p.wait_ns) ? 1 : 0;
+            __syncwarp();
+            ok = __shfl_sync(FULL, ok, 0);
+            if (!ok) {
+                if (lane == 0) set_dev_error(p.ctrl, DEV_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const int4 d = adesc[a];
+            if (d.x == DESC_END) break;
+            const int grp = d.x, r = d.y, valid = d.z;
+            const bool any = 32 * w4 < valid;  // warp-uniform
+            // the NP partials of each head's score, summed in fp32 (round to nearest) as a tree
+            float part[NP][G];
+            if (any) {
+#pragma unroll
+                for (int pp = 0; pp < NP; ++pp) {
+                    uint32_t v[G];
+                    tmem_ld32<G>(tbase + ((uint32_t)(32 * w4) << 16) + (uint32_t)(a * UCOLS + pp * SC_N), v);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) part[pp][h] = __uint_as_float(v[h]);
+                }
+#pragma unroll
+                for (int st = 1; st < NP; st <<= 1)
+#pragma unroll
+                    for (int pp = 0; pp + st < NP; pp += 2 * st)
+#pragma unroll
+                        for (int h = 0; h < G; ++h) part[pp][h] = __fadd_rn(part[pp][h], part[pp + st][h]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[a]);
+            if (!any) continue;
+
+            const int key = 32 * w4 + lane;   // key of the unit held by this lane
+            const bool kv = key < valid;
+            const size_t chunk = (size_t)r * (SC_M / CHUNK) + w4;
+            const size_t bh0 = (size_t)grp * G;  // first query head of the group: b*H_q + g*G
+            float sv[G], mx[G], ct[G], tot[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const uint4 a = *reinterpret_cast<const uint4 *>(qg + h * D + 8 * sub);
-                const uint4 c = *reinterpret_cast<const uint4 *>(qg + h * D + 8 * (sub + C::P));
-                const uint32_t wv[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i) qp[h][i] = bf16x2_to_f32x2(wv[i]);
+                sv[h] = part[0][h];
+                mx[h] = kv ? __fmul_rn(sv[h], p.k2_hi) : NEG_INF;
             }
-        }
-
-        // ---- dot products: call c covers keys [c*KW, c*KW + KW) of the tile
-        const uint8_t *tb = ring + slot * T::BYTES;
-        float sc[NCALL][NV];
+            // the chunk's maximum (log2 units) and its scale c_t
 #pragma unroll
-        for (int c = 0; c < NCALL; ++c) {
-            float val[2 * G];
-            tile_dots<D, G>(tb, c * C::KW + 2 * grp, sub, qp, val);
+            for (int o = 16; o >= 1; o >>= 1)
 #pragma unroll
-            for (int i = 0; i < NV; ++i) sc[c][i] = val[i];
-        }
-        __syncwarp();
-        produce(slot, it);  // the tile and the query heads are in registers: refill the slot
-
-        // ---- the chunk's maximum (log2 units) and its scale c_t
-        const bool own = (sub % C::REP) == 0;
-        float tmx[NV], ct[NV];
+                for (int h = 0; h < G; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(FULL, mx[h], o));
+            // weights (stored) and the chunk totals
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            float m = NEG_INF;
-#pragma unroll
-            for (int c = 0; c < NCALL; ++c) {
-                const int key = c * C::KW + 2 * grp + C::key2_of(lane, i);
-                if (key < rows) m = fmaxf(m, __fmul_rn(sc[c][i], p.k2_hi));
+            for (int h = 0; h < G; ++h) {
+                ct[h] = ceilf(fminf(fmaxf(mx[h], -16777216.f), 16777216.f));
+                float w = 0.f;
+                if (kv) {
+                    w = exp2f(__fmaf_rn(sv[h], p.k2_lo, __fmaf_rn(sv[h], p.k2_hi, -ct[h])));
+                    st_hint(p.w + (bh0 + h) * p.n_pad + chunk * CHUNK + lane, w, keep);
+                }
+                tot[h] = w;
             }
 #pragma unroll
-            for (int msk = 1; msk < 32; msk <<= 1)
-                if (C::SAME & (unsigned)msk) m = fmaxf(m, __shfl_xor_sync(FULL, m, msk));
-            tmx[i] = m;
-            ct[i] = ceilf(fminf(fmaxf(m, -16777216.f), 16777216.f));
-        }
-
-        // ---- weights (stored) and the chunk totals
-        const size_t bh0 = (size_t)grpid * G;  // first query head of the group: b*H_q + g*G
-        const size_t chunk = (size_t)ur_c * (L / CHUNK) + (size_t)tile;  // chunk index in the sequence
-        float tot[NV];
+            for (int o = 16; o >= 1; o >>= 1)
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int h = C::head_of(lane, i);
-            float *wrow = p.w + (bh0 + h) * p.n_pad + chunk * CHUNK;
-            float acc = 0.f;
+                for (int h = 0; h < G; ++h) tot[h] = __fadd_rn(tot[h], __shfl_xor_sync(FULL, tot[h], o));
+            // lane h records head h's chunk
 #pragma unroll
-            for (int c = 0; c < NCALL; ++c) {
-                const int key = c * C::KW + 2 * grp + C::key2_of(lane, i);
-                if (key < rows) {
-                    const float e = __fmaf_rn(sc[c][i], p.k2_lo, __fmaf_rn(sc[c][i], p.k2_hi, -ct[i]));
-                    const float w = exp2f(e);
-                    if (own) {
-                        st_hint(wrow + key, w, keep);
-                        acc = __fadd_rn(acc, w);
-                    }
+            for (int h = 0; h < G; ++h) {
+                if (lane == h) {
+                    const size_t ci = (bh0 + h) * p.nch + chunk;
+                    st_hint(p.ctot + ci, tot[h], keep);
+                    st_hint(p.cexp + ci, (int)ct[h], keep);
+                    st_hint(p.cmax + ci, mx[h], keep);
                 }
             }
-#pragma unroll
-            for (int msk = 1; msk < 32; msk <<= 1)
-                if (C::SAME & (unsigned)msk) acc = __fadd_rn(acc, __shfl_xor_sync(FULL, acc, msk));
-            tot[i] = acc;
-        }
-        // one lane per head records the chunk (lane bits outside SAME select the head)
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            if ((lane & C::SAME) == 0 && own) {
-                const size_t ci = (bh0 + C::head_of(lane, i)) * p.nch + chunk;
-                st_hint(p.ctot + ci, tot[i], keep);
-                st_hint(p.cexp + ci, (int)ct[i], keep);
-                st_hint(p.cmax + ci, tmx[i], keep);
-            }
         }
     }
 
-    if (aborted) {
-        // give the copies still in flight a bounded chance to land before the CTA exits
-        if (lane == 0) {
-            set_dev_error(p.ctrl, DEV_TIMEOUT);
-            for (int k = 0; k < NSTAGE; ++k) {
-                const int j = it + k;
-                if (desc[j % NSTAGE].x != DESC_END)
-                    mbar_wait_bounded(&bars[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u, p.wait_ns);
-            }
-        }
-        __syncwarp();
+    // ---- teardown: every MMA has completed (drained above); release TMEM.  After a
+    // timeout, fills the MMA thread never consumed get a bounded wait to land first.
+    tc_fence_before();
+    __syncthreads();
+    if (warp == SC_WARP_PROD && lane == 0) {
+        const int nfill = (int)tmem_slot[2];
+        for (int f = (int)tmem_slot[1]; f < nfill; ++f)
+            if (!mbar_wait_bounded(&full[f % NS], (uint32_t)(f / NS) & 1u, p.wait_ns)) break;
+    }
+    if (warp == SC_WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tbase, SC_TMEM_COLS);
     }
     __threadfence();
-    __syncthreads();
     pdl_launch_dependents();
     if (tid == 0) {
         const int done = atomicAdd(p.ctrl + CTRL_EXIT, 1);

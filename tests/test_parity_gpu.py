@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from stochastic_sparse_kv_gb300 import santa, workloads
-from tests.parity_util import check_dense, check_estimator, check_indices
+from tests.parity_util import MISMATCH_FRAC, check_dense, check_estimator, check_indices, count_mismatches
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -216,6 +216,40 @@ def test_ragged_b32_heavy_hitters_sampled_pairs():
 @pytest.mark.slow
 def test_long_context_131k_sampled_pairs():
     print(_full_check(workloads.LONG[2], ("systematic", "stratified", "dense"), n_pairs=12))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("case", ["d64_140k", "llama_b4_131k"])
+def test_boundary_mismatch_rate_pooled(case):
+    """The boundary-mismatch rate, pooled over seeds, both sampling modes and every
+    (b, h): more than 100k points per case, strictly below 0.1%.  Long sequences are
+    where fp32 rounding of the score stage moves CDF boundaries most (the oracle's CDF
+    is exact fp64)."""
+    if case == "d64_140k":
+        _, q, k, v, sl = workloads.small("case", 2, 8, 2, 64, 140000, 200, seq_lens=[140000, 3000],
+                                         seed=64 + 8 + 140000)
+        S, seeds = 200, range(16)
+    else:
+        q, k, v, sl = workloads.make_inputs(workloads.LONG[2])
+        S, seeds = 256, range(2)
+    qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
+    W_cache = {}
+    nm = npts = 0
+    for mode in ("systematic", "stratified"):
+        for seed in seeds:
+            _, idx = santa.decode(qd, kd, vd, sld, S, mode, seed=seed)
+            torch.cuda.synchronize()
+            idx = idx.cpu().numpy()
+            _, i_ref = oracle.decode(q, k, v, sl, S, mode, seed=seed)
+            pairs = [(b, h) for b in range(idx.shape[0]) for h in range(idx.shape[1]) if int(sl[b]) > 0]
+            m, n = count_mismatches(idx, i_ref, q, k, sl, S, mode, seed, pairs, W_cache)
+            nm += m
+            npts += n
+    del qd, kd, vd
+    torch.cuda.empty_cache()
+    print(f"{case}: {nm} boundary mismatches of {npts} points ({nm / npts:.4%})")
+    assert npts >= 100000
+    assert nm < MISMATCH_FRAC * npts, f"{nm} boundary mismatches of {npts} points"
 
 
 # ------------------------------------------------------------------ unbiasedness
