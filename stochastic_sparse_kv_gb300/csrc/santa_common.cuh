@@ -193,6 +193,18 @@ __device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint3
                  : "memory");
 }
 
+// Drop the 128-byte L2 lines lying wholly inside [base, base + bytes) without writing
+// them back: their data becomes undefined.  For scratch that has been read for the last
+// time, so that dirty lines are not evicted to DRAM later.  Threads tid of nt share it.
+__device__ __forceinline__ void l2_discard_range(const void *base, size_t bytes, int tid, int nt)
+{
+    const size_t g = __cvta_generic_to_global(base);
+    const size_t a0 = (g + 127) & ~(size_t)127;
+    const size_t a1 = (g + bytes) & ~(size_t)127;
+    for (size_t a = a0 + (size_t)tid * 128; a < a1; a += (size_t)nt * 128)
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(a) : "memory");
+}
+
 // ------------------------------------------------------------------ arithmetic
 
 // bf16 pair (low element in the low half) -> packed fp32 pair, exact.

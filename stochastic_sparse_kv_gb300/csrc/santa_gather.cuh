@@ -366,6 +366,13 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
         idx[s] = j0 + pick;            // (iid: overwrites this point's own uniform)
     }
     __syncthreads();
+    // The head's weights and chunk data have been read for the last time: drop them from
+    // L2 so that they are never written back (the next step's score stage rewrites them).
+    l2_discard_range(wrow, (size_t)nchn * CHUNK * sizeof(float), tid, NT);
+    l2_discard_range(p.ctot + bhc, (size_t)p.nch * sizeof(float), tid, NT);
+    l2_discard_range(p.cexp + bhc, (size_t)p.nch * sizeof(int), tid, NT);
+    l2_discard_range(p.cmax + bhc, (size_t)p.nch * sizeof(float), tid, NT);
+    if (!in_smem) l2_discard_range(p.cpre + bhc, (size_t)p.nch * sizeof(uint64_t), tid, NT);
 
     // ---- G. sorted indices out; each warp gathers the distinct rows of its run of
     // points (a row split between two warps is loaded by both, each with its own count)
