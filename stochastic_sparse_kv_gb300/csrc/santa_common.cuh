@@ -205,6 +205,12 @@ __device__ __forceinline__ void l2_discard_range(const void *base, size_t bytes,
         asm volatile("discard.global.L2 [%0], 128;" ::"l"(a) : "memory");
 }
 
+// Fetch the 128-byte line holding p into L2 (no register result, nothing waits on it).
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(__cvta_generic_to_global(p)));
+}
+
 // ------------------------------------------------------------------ arithmetic
 
 // bf16 pair (low element in the low half) -> packed fp32 pair, exact.

@@ -243,32 +243,42 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
         __syncthreads();
     }
 
-    // ---- C. heavy keys of the hot chunks: slot q = hot entry * 32 + key; eight loads in
-    // flight per thread before any of them is acted on
+    // ---- C. heavy keys of the hot chunks: slot q = hot entry * 8 + quarter (four keys,
+    // one 16-byte load); up to eight loads in flight per thread before any is acted on,
+    // so HCAP hot chunks take one round.
     float *wrow = p.w + (size_t)bh * p.n_pad;
-    for (int q0 = tid; q0 < nhot * CHUNK; q0 += 8 * NT) {
-        float wv[8];
+    const uint16_t *kg = p.k + ((size_t)b * p.H_kv + g) * (size_t)p.n_max * D;
+    constexpr int QPC = CHUNK / 4;  // quarters per chunk
+    for (int q0 = tid; q0 < nhot * QPC; q0 += 8 * NT) {
+        float4 wv[8];
         int jj[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int q = q0 + u * NT;
             jj[u] = -1;
-            wv[u] = 0.f;
-            if (q < nhot * CHUNK) {
-                const int j = hot[q / CHUNK] * CHUNK + (q % CHUNK);
+            wv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (q < nhot * QPC) {
+                const int j = hot[q / QPC] * CHUNK + (q % QPC) * 4;
                 if (j < n) {
                     jj[u] = j;
-                    wv[u] = __ldcg(wrow + j);
+                    wv[u] = __ldcg(reinterpret_cast<const float4 *>(wrow + j));
                 }
             }
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            if (jj[u] >= 0 && wv[u] >= exp2f(thr - (float)cexp[jj[u] / CHUNK])) {
-                const int pos = atomicAdd(misc + GM_NHV, 1);
-                if (pos < HKCAP) {
-                    hv[pos] = jj[u];
-                    hvw[pos] = wv[u];
+            if (jj[u] < 0) continue;
+            const float wt = exp2f(thr - (float)cexp[jj[u] / CHUNK]);
+            const float w4[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = jj[u] + e;
+                if (j < n && w4[e] >= wt) {
+                    const int pos = atomicAdd(misc + GM_NHV, 1);
+                    if (pos < HKCAP) {
+                        hv[pos] = j;
+                        hvw[pos] = w4[e];
+                    }
                 }
             }
         }
@@ -277,7 +287,6 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
     const int nhv = min(misc[GM_NHV], HKCAP);
 
     // ---- D. re-score the heavy keys (four lanes each) and patch their chunk totals
-    const uint16_t *kg = p.k + ((size_t)b * p.H_kv + g) * (size_t)p.n_max * D;
     for (int i0 = 0; i0 < nhv; i0 += NT / 4) {  // (every lane runs every pass: they shuffle)
         const int i = i0 + tid / 4, part = tid & 3;
         const int j = i < nhv ? hv[i] : 0;
@@ -364,6 +373,10 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
         }
         if (pick < 0) pick = lastpos;  // only when rounding put t past the chunk's mass
         idx[s] = j0 + pick;            // (iid: overwrites this point's own uniform)
+        // the V row this point selects: into L2 now, gathered in G
+        const uint16_t *vrow = p.v + (((size_t)b * p.H_kv + g) * (size_t)p.n_max + (size_t)(j0 + pick)) * D;
+        prefetch_l2(vrow);
+        if (D * 2 > 128) prefetch_l2(vrow + 64);
     }
     __syncthreads();
     // The head's weights and chunk data have been read for the last time: drop them from
