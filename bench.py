@@ -35,6 +35,7 @@ KERNEL_SOURCES = [os.path.join(CSRC, f) for f in ("santa_common.cuh", "santa_sam
 # The sampled path is two launches chained by programmatic dependent launch (the value
 # stage overlaps the score kernel's tail), so one santa_decode call is timed as the unit.
 ROOFLINE_UNIT = "santa_decode: santa_score_kernel<128,4> + santa_gather_kernel<128> (PDL-chained)"
+ROOFLINE_UNIT_DENSE = "santa_decode (dense): santa_dense_kernel<128,4> + santa_dense_merge_kernel<128> (PDL-chained)"
 
 
 def log(*a):
@@ -279,7 +280,8 @@ def run_ours(args):
         cpu = cpu_baseline(q, k, v, sl, w, S, mode, args.cpu_rows)
 
     if rank == 0:
-        traffic = profiled_traffic()
+        # the committed DRAM record covers the sampled path's launch pair only
+        traffic = profiled_traffic() if mode != "dense" else None
         rec = {
             "metric": METRIC, "value": round(us_step, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_step / 1000, 5),
@@ -290,11 +292,12 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
-                         "kernel": ROOFLINE_UNIT, "algorithmic_bytes_per_launch": abytes,
+                         "kernel": ROOFLINE_UNIT_DENSE if mode == "dense" else ROOFLINE_UNIT,
+                         "algorithmic_bytes_per_launch": abytes,
                          "avg_launch_us": round(avg_launch_ms * 1000, 2)},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps * (1 if mode == "dense" else 2),
+            "gpu_launches": args.steps * 2,  # score + value stage, or dense + merge
             "clocks": clocks,
             "modes": modes,
             "S_sweep_systematic": sweep,

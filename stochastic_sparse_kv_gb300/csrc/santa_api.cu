@@ -284,8 +284,8 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     if ((rc = device_info(&dev, &sms, &optin))) return rc;
     const int D = shape->d, G = shape->H_q / shape->H_kv;
     const int L = dense ? DENSE_UNIT : SC_M;  // keys per work unit
-    // the score kernel addresses K rows with 32-bit TMA coordinates
-    if (!dense && (long long)shape->B * shape->H_kv * shape->n_max >= (1ll << 31)) return SANTA_ERR_UNSUPPORTED;
+    // the kernels address K and V rows with 32-bit TMA coordinates
+    if ((long long)shape->B * shape->H_kv * shape->n_max >= (1ll << 31)) return SANTA_ERR_UNSUPPORTED;
 
     Params p{};
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -330,7 +330,7 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     if (!fn) return SANTA_ERR_UNSUPPORTED;
     const int smem = dense ? dense_smem_bytes(D, G, shape->B) : score_smem_bytes(D, G, shape->B);
     if (smem > optin) return SANTA_ERR_UNSUPPORTED;
-    const int threads = dense ? NT : SC_NT;
+    const int threads = dense ? DN_NT : SC_NT;
     int occ = 0;
     if ((rc = prepare_fn(fn, dev, smem, threads, &occ))) return rc;
     const void *fn2 = nullptr;
@@ -348,15 +348,38 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;
     void *args[] = {&p};
+    const long long krows = (long long)shape->B * shape->H_kv * shape->n_max;
     if (dense) {
-        if (cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(NT), args, (size_t)smem, (cudaStream_t)stream) !=
+        // K and V as [B*H_kv*n_max][d] in boxes of a subunit (SC_M rows) and of SC_BOX_ROWS
+        // rows (a split's last keys); q in boxes of one group's G heads
+        CUtensorMap tm_k, tm_kt, tm_v, tm_vt, tm_q;
+        if ((rc = make_map_bf16(&tm_k, k_cache, D, krows, SC_M))) return rc;
+        if ((rc = make_map_bf16(&tm_kt, k_cache, D, krows, SC_BOX_ROWS))) return rc;
+        if ((rc = make_map_bf16(&tm_v, v_cache, D, krows, SC_M))) return rc;
+        if ((rc = make_map_bf16(&tm_vt, v_cache, D, krows, SC_BOX_ROWS))) return rc;
+        if ((rc = make_map_bf16(&tm_q, q, D, (long long)shape->B * shape->H_q, G))) return rc;
+        void *dargs[] = {&p, &tm_k, &tm_kt, &tm_v, &tm_vt, &tm_q};
+        if (cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(DN_NT), dargs, (size_t)smem, (cudaStream_t)stream) !=
             cudaSuccess)
             return SANTA_ERR_CUDA;
+        // the merge of the split partials, one CTA per (b, h_q), as a programmatic dependent
+        const void *fm = (D == 128) ? kernel_d128(KIND_DMERGE, G) : kernel_d64(KIND_DMERGE, G);
+        if (!fm) return SANTA_ERR_UNSUPPORTED;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)(shape->B * shape->H_q));
+        cfg.blockDim = dim3((unsigned)D);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = (cudaStream_t)stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelExC(&cfg, fm, args) != cudaSuccess) return SANTA_ERR_CUDA;
     } else {
         // K as [B*H_kv*n_max][d] in boxes of a whole unit (SC_M rows) and of SC_BOX_ROWS rows
         // (a sequence's last unit); q as [B*H_q][d] in boxes of one group's G heads
         CUtensorMap tm_k, tm_kt, tm_q;
-        const long long krows = (long long)shape->B * shape->H_kv * shape->n_max;
         if ((rc = make_map_bf16(&tm_k, k_cache, D, krows, SC_M))) return rc;
         if ((rc = make_map_bf16(&tm_kt, k_cache, D, krows, SC_BOX_ROWS))) return rc;
         if ((rc = make_map_bf16(&tm_q, q, D, (long long)shape->B * shape->H_q, G))) return rc;

@@ -2,398 +2,504 @@
 //
 // Exact softmax attention o = sum_j p_j v_j: the quantity SANTA estimates ("Stochastic
 // Sparse Attention for Memory-Bound Inference", abstract; the pages compare against
-// split-K decode kernels).  Built like the score kernel of the sampled path, so that
-// the comparison is like for like:
+// split-K decode kernels).  Built on the score kernel's machinery, so that the
+// comparison is like for like:
 //
-//  * persistent CTAs of 8 independent warps; a warp takes work units of UNIT keys of one
-//    (b, g) -- a static contiguous block first, then shrinking grabs from a counter --
-//    and streams K and V tiles of KEYS keys through its own ring of TMA bulk copies;
-//  * per tile: the G query heads' scores (tile_dots), an online softmax per head (running
-//    maximum m and sum l in log2 units, with rescaling when m grows), and p.V with the
-//    tile's probabilities broadcast through shared memory; each lane owns D/32 output
-//    dimensions of every head;
-//  * at the end of a unit the warp writes its partial (m, l, o) per head; the warp that
-//    completes the last unit of a group merges the group's partials into `out`.
+//  * persistent CTAs, one per SM: one thread streams K, V and the group's query rows
+//    with tiled TMA copies into a ring of stages (a stage = 128 keys of one (b, g)); one
+//    thread issues q.K^T on the tensor cores (tcgen05, each K step into its own TMEM
+//    partial); one warpgroup of four epilogue warps does the rest in fp32 on the CUDA
+//    cores: the scores' online softmax per head, and p.V with V read from the stage
+//    (each lane owns D/32 output dimensions of every head, p broadcast through shared
+//    memory);
+//  * the work items are splits of DENSE_UNIT keys (a static contiguous block per CTA,
+//    then shrinking grabs); the four warps combine their running (m, l, o) at the end of
+//    a split and write one partial per (head, split);
+//  * santa_dense_merge_kernel, a programmatic dependent launch, combines a head's
+//    partials into `out` (the log-sum-exp merge of split-K decoding).
 #pragma once
 
-#include "santa_sample.cuh"
+#include "santa_score.cuh"
 
 namespace santa {
 
-template <int D, int G>
-struct DenseTile {
-    static constexpr int KEYS = (D == 128) ? 16 : 32;  // keys per tile (a multiple of tile_dots' KW)
-    static constexpr int KVB = KEYS * 2 * D;           // bytes of the tile's K (or V) part: 4 KB
-    static constexpr int NSTAGE = 3;
-    static constexpr int QBYTES = G * D * 2;
-    static constexpr int UNIT = DENSE_UNIT;            // keys per work unit
-    static constexpr int EPL = D / 32;                 // output dimensions per lane
-};
+constexpr int DN_WARP_PROD = 4;        // TMA producer
+constexpr int DN_WARP_MMA = 5;         // MMA issuer, owner of the TMEM allocation
+constexpr int DN_NT = 192;             // threads per CTA: four epilogue warps, producer, MMA
+constexpr int DN_RING_BYTES = 208896;  // K, V and query stages
+constexpr int DN_HROUND = 4;           // heads combined per round at the end of a split
+enum : int { DF_FIRST = 1, DF_LAST = 2 };  // descriptor flags: first / last subunit of a split
+
+__host__ __device__ constexpr int dense_stages(int D)
+{
+    return DN_RING_BYTES / (2 * score_kbytes(D) + score_qbytes(D));
+}
 
 struct DenseSmem {
-    int nb, prefix, misc, warp0, warp_bytes, ring, qbuf, pbuf, bar, desc, total;
+    int kst, vst, qst, bar, desc, adesc, tmem, pk, comb, nb, prefix, total;
 };
 
+// Byte offsets from the 1024-aligned base; `total` includes the alignment slack.
 __host__ __device__ inline DenseSmem dense_smem(int D, int G, int B)
 {
-    const int keys = (D == 128) ? 16 : 32;
-    const int kvb = keys * 2 * D;
-    const int nstage = 3;
+    const int ns = dense_stages(D), nacc = score_nacc(D);
+    const int hr = G < DN_HROUND ? G : DN_HROUND;
     DenseSmem s{};
     int off = 0;
+    s.kst = off; off += ns * score_kbytes(D);
+    s.vst = off; off += ns * score_kbytes(D);
+    s.qst = off; off += ns * score_qbytes(D);
+    s.bar = off; off += (int)align_up((size_t)(2 * ns + 2 * nacc + 2) * 8, 16);
+    s.desc = off; off += ns * 16;
+    s.adesc = off; off += nacc * 16;
+    s.tmem = off; off += 16;
+    s.pk = off; off += 4 * 32 * G * 4;                                     // per warp: p[32 keys][G]
+    s.comb = off; off += (int)align_up((size_t)4 * hr * (D + 2) * 4, 16);  // [warp][head][m, l, o[D]]
     s.nb = off; off += (int)align_up((size_t)B * 4, 16);
     s.prefix = off; off += (int)align_up((size_t)(B + 1) * 4, 16);
-    s.misc = off; off += 16 * 4;
-    s.warp0 = (int)align_up((size_t)off, 128);
-    int w = 0;
-    s.ring = w; w += nstage * 2 * kvb;
-    s.qbuf = w; w += G * D * 2;
-    s.pbuf = w; w += keys * G * 4 + G * 4;  // the tile's p[key][head], then alpha[head]
-    s.bar = w = (int)align_up((size_t)w, 8); w += nstage * 8;
-    s.desc = w = (int)align_up((size_t)w, 16); w += nstage * 16;
-    s.warp_bytes = (int)align_up((size_t)w, 128);
-    s.total = s.warp0 + NWARP * s.warp_bytes;
+    s.total = off + 1024;
     return s;
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(NT, 1) santa_dense_kernel(const Params p)
+__global__ void __launch_bounds__(DN_NT, 1)
+    santa_dense_kernel(const Params p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_kt,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_vt,
+                       const __grid_constant__ CUtensorMap tm_q)
 {
-    using C = SampleCfg<D, G>;
-    using T = DenseTile<D, G>;
-    constexpr int NSTAGE = T::NSTAGE;
-    constexpr int NCALL = T::KEYS / C::KW;  // tile_dots calls per tile
-    constexpr int NV = C::NV;
-    constexpr int EPL = T::EPL;
-    constexpr int L = T::UNIT;
+    constexpr int NH = score_halves(D);
+    constexpr int KB = SC_M * 128;   // one 128-byte column block of a K or V tile: 16 KB
+    constexpr int QB = SC_N * 128;   // one column block of the query tile: 2 KB
+    constexpr int NS = dense_stages(D);
+    constexpr int CH = score_chain(D);
+    constexpr int NP = score_parts(D);
+    constexpr int UCOLS = score_ucols(D);
+    constexpr int NACC = score_nacc(D);
+    constexpr int EPL = D / 32;              // output dimensions per lane
+    constexpr int L = DENSE_UNIT;            // keys per split (one partial)
+    constexpr int HR = G < DN_HROUND ? G : DN_HROUND;
+    constexpr uint32_t IDESC = idesc_bf16_f32(SC_M, SC_N);
     constexpr unsigned FULL = 0xffffffffu;
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int sub = lane % C::P, grp = lane / C::P;
-    const int B = p.B, H_kv = p.H_kv, H_q = p.H_q;
+    static_assert(G >= 1 && G <= 8 && SC_N >= G, "query heads per group");
+    static_assert(NS >= 2 && NACC >= 2, "stage ring and accumulators");
+    static_assert(L % SC_M == 0, "a split is whole subunits");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const int B = p.B, H_kv = p.H_kv;
     const DenseSmem lay = dense_smem(D, G, B);
+    uint8_t *kst = smem + lay.kst;
+    uint8_t *vst = smem + lay.vst;
+    uint8_t *qst = smem + lay.qst;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar);
+    uint64_t *empty = full + NS;
+    uint64_t *tfull = empty + NS;
+    uint64_t *tempty = tfull + NACC;
+    uint64_t *drain = tempty + NACC;
+    uint64_t *wgbar = drain + 1;
+    int4 *desc = reinterpret_cast<int4 *>(smem + lay.desc);
+    int4 *adesc = reinterpret_cast<int4 *>(smem + lay.adesc);
+    // [0] the TMEM address, [1] full phases the MMA thread consumed, [2] stages filled
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + lay.tmem);
+    float *pk = reinterpret_cast<float *>(smem + lay.pk);
+    float *comb = reinterpret_cast<float *>(smem + lay.comb);
     int *nb = reinterpret_cast<int *>(smem + lay.nb);
     int *prefix = reinterpret_cast<int *>(smem + lay.prefix);
-    int *misc = reinterpret_cast<int *>(smem + lay.misc);
-    uint8_t *wb = smem + lay.warp0 + warp * lay.warp_bytes;
-    uint8_t *ring = wb + lay.ring;
-    uint8_t *qbuf = wb + lay.qbuf;
-    float *pk = reinterpret_cast<float *>(wb + lay.pbuf);  // [KEYS][G], then alpha[G]
-    float *alpha_s = pk + T::KEYS * G;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(wb + lay.bar);
-    int4 *desc = reinterpret_cast<int4 *>(wb + lay.desc);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float NEG_INF = __int_as_float(0xff800000);
 
-    // the work units: UNIT keys per (b, g, r), counted per batch row like the score kernel's
-    Params pu = p;
-    pu.L = L;
-    build_item_space(pu, nb, prefix, misc);
-    if (lane == 0) {
-        for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
-        mbar_fence_init();
+    // ---- setup: TMEM, barriers, the work-item space, zero padding rows of the query tiles
+    if (warp == DN_WARP_MMA) {
+        tmem_alloc(tmem_slot, SC_TMEM_COLS);
+        tmem_relinquish();
     }
-    __syncthreads();  // the only CTA-wide barrier
-    const int total_items = prefix[B];
-    const int W = (int)gridDim.x * NWARP;
-    const int gw = (int)blockIdx.x * NWARP + warp;
-    const int Ks = (int)((long long)total_items * 4 / 5 / W);  // static units per warp
-    const int dyn0 = Ks * W;
-
-    // ---- producer (warp-uniform; lane 0 issues the copies and the atomics)
-    uint64_t policy = 0;
-    int pend = 0;  // lane 0: the outstanding grab, first unit * 8 + size
-    auto request = [&](int last) {
+    if (warp == DN_WARP_PROD) {
         if (lane == 0) {
-            const int k = max(1, min(4, (total_items - last) / (2 * W)));
-            pend = (dyn0 + atomicAdd(p.ctrl + CTRL_WORK, k)) * 8 + k;
-        }
-    };
-    if (lane == 0) policy = l2_policy_evict_first();
-    request(dyn0);
-    int g_next = gw * Ks, g_end = g_next + Ks;  // the current grab: the static block first
-    int pr_r = 0, pr_tile = 0, pr_ntiles = 0, pr_valid = 0, pr_grp = 0, pr_group = -1, pr_seq = 0;
-    int q_issue = -1;  // sequence number of the tile that carried the staged query heads
-    long long pr_row0 = 0;
-    bool pr_end = false;
-    int ub = 0, ug = 0, ur = 0, uns = 1;  // position of unit g_next
-    auto seek = [&](int itm) {
-        const Item x = decode_item(itm, prefix, nb, B, H_kv, L);
-        ub = x.b;
-        ug = x.g;
-        ur = x.r;
-        uns = x.ns;
-    };
-    auto step = [&]() {
-        if (++ur == uns) {
-            ur = 0;
-            if (++ug == H_kv) {
-                ug = 0;
-                if (++ub < B) uns = nb[ub] > 0 ? (nb[ub] + L - 1) / L : 1;
+            tmem_slot[1] = 0;
+            tmem_slot[2] = 0;
+            tma_prefetch_map(&tm_k);
+            tma_prefetch_map(&tm_kt);
+            tma_prefetch_map(&tm_v);
+            tma_prefetch_map(&tm_vt);
+            tma_prefetch_map(&tm_q);
+            for (int s = 0; s < NS; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], 4);  // the four epilogue warps, after their V reads
             }
+            for (int a = 0; a < NACC; ++a) {
+                mbar_init(&tfull[a], 2);   // the MMA commit and the issuing thread
+                mbar_init(&tempty[a], 4);  // the four epilogue warps
+            }
+            mbar_init(drain, 1);
+            mbar_init(wgbar, 4);           // the epilogue warps' own rendezvous
+            mbar_fence_init();
         }
-    };
-    if (g_next < g_end) seek(g_next);
-    auto produce = [&](int slot, int cons_seq) {
-        while (!pr_end && pr_tile == pr_ntiles) {
-            if (g_next == g_end) {
-                const int got = __shfl_sync(FULL, pend, 0);
-                g_next = got >> 3;
-                g_end = min(g_next + (got & 7), total_items);
-                if (g_next >= total_items) {
-                    pr_end = true;
+        warp_item_space(p, L, nb, prefix);
+    }
+    {
+        constexpr int PIECES = (SC_N - G) * 8;  // 16-byte pieces per column block
+        for (int i = tid; i < NS * NH * PIECES; i += DN_NT) {
+            const int blk = i / PIECES, rem = i % PIECES;
+            *reinterpret_cast<uint4 *>(qst + blk * QB + (G + rem / 8) * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == DN_WARP_PROD) {
+        // ================= producer: one thread streams K, V and the group's queries
+        if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();
+            const int total_items = prefix[B];
+            const int W = (int)gridDim.x;
+            const int Ks = (int)((long long)total_items * 4 / 5 / W);  // static splits per CTA
+            const int dyn0 = Ks * W;
+            auto request = [&](int last) {
+                const int k = max(1, min(4, (total_items - last) / (2 * W)));
+                return (dyn0 + atomicAdd(p.ctrl + CTRL_WORK, k)) * 8 + k;
+            };
+            int pend = request(dyn0);
+            int g_next = (int)blockIdx.x * Ks, g_end = g_next + Ks;
+            int ub = 0, ug = 0, ur = 0, uns = 1;
+            auto seek = [&](int itm) {
+                const Item x = decode_item(itm, prefix, nb, B, H_kv, L);
+                ub = x.b;
+                ug = x.g;
+                ur = x.r;
+                uns = x.ns;
+            };
+            if (g_next < g_end) seek(g_next);
+            int i = 0;  // stages filled
+            bool stop = false;
+            while (!stop) {
+                // the next split with keys, or the end of the work
+                int n = 0, b = 0, g = 0, r = 0;
+                bool have = false;
+                while (!have) {
+                    if (g_next == g_end) {
+                        g_next = pend >> 3;
+                        g_end = min(g_next + (pend & 7), total_items);
+                        if (g_next >= total_items) break;
+                        pend = request(g_end);
+                        seek(g_next);
+                    }
+                    n = nb[ub];
+                    b = ub;
+                    g = ug;
+                    r = ur;
+                    ++g_next;
+                    if (++ur == uns) {
+                        ur = 0;
+                        if (++ug == H_kv) {
+                            ug = 0;
+                            if (++ub < B) uns = nb[ub] > 0 ? (nb[ub] + L - 1) / L : 1;
+                        }
+                    }
+                    have = n > 0;  // empty rows: the merge kernel writes their zeros
+                }
+                const int vsplit = have ? min(L, n - r * L) : 0;
+                const int nsub = have ? (vsplit + SC_M - 1) / SC_M : 1;
+                for (int u = 0; u < nsub; ++u, ++i) {
+                    const int s = i % NS;
+                    if (!mbar_wait_bounded(&empty[s], ((uint32_t)(i / NS) & 1u) ^ 1u, p.wait_ns)) {
+                        set_dev_error(p.ctrl, DEV_TIMEOUT);
+                        stop = true;
+                        break;
+                    }
+                    if (!have) {
+                        desc[s] = make_int4(DESC_END, 0, 0, 0);
+                        mbar_arrive(&full[s]);
+                        ++i;
+                        stop = true;
+                        break;
+                    }
+                    const int valid = min(SC_M, vsplit - u * SC_M);
+                    const int grp = b * H_kv + g;
+                    desc[s] = make_int4(grp, r, valid, (u << 8) | (u == 0 ? DF_FIRST : 0) | (u == nsub - 1 ? DF_LAST : 0));
+                    const int row0 = grp * p.n_max + r * L + u * SC_M;
+                    uint8_t *kt = kst + s * NH * KB;
+                    uint8_t *vt = vst + s * NH * KB;
+                    if (valid == SC_M) {
+                        mbar_arrive_tx(&full[s], (uint32_t)(2 * NH * KB + NH * G * 128));
+#pragma unroll
+                        for (int hf = 0; hf < NH; ++hf) {
+                            tma_load_2d(kt + hf * KB, &tm_k, hf * 64, row0, &full[s], policy);
+                            tma_load_2d(vt + hf * KB, &tm_v, hf * 64, row0, &full[s], policy);
+                        }
+                    } else {
+                        const int nbox = (valid + SC_BOX_ROWS - 1) / SC_BOX_ROWS;
+                        mbar_arrive_tx(&full[s], (uint32_t)(2 * nbox * NH * SC_BOX_ROWS * 128 + NH * G * 128));
+                        for (int jb = 0; jb < nbox; ++jb)
+#pragma unroll
+                            for (int hf = 0; hf < NH; ++hf) {
+                                const int off = hf * KB + jb * SC_BOX_ROWS * 128, y = row0 + jb * SC_BOX_ROWS;
+                                tma_load_2d(kt + off, &tm_kt, hf * 64, y, &full[s], policy);
+                                tma_load_2d(vt + off, &tm_vt, hf * 64, y, &full[s], policy);
+                            }
+                    }
+#pragma unroll
+                    for (int hf = 0; hf < NH; ++hf)
+                        tma_load_2d_plain(qst + (s * NH + hf) * QB, &tm_q, hf * 64, grp * G, &full[s]);
+                }
+            }
+            tmem_slot[2] = (uint32_t)i;
+        }
+        __syncwarp();
+    } else if (warp == DN_WARP_MMA) {
+        // ================= MMA issuer: one thread; accumulator a = stage fill % NACC
+        if (lane == 0) {
+            int j = 0;
+            for (;; ++j) {
+                const int s = j % NS, a = j % NACC;
+                if (!mbar_wait_bounded(&full[s], (uint32_t)(j / NS) & 1u, p.wait_ns)) {
+                    set_dev_error(p.ctrl, DEV_TIMEOUT);
                     break;
                 }
-                request(g_end);
-                seek(g_next);
-            }
-            const int n = nb[ub];
-            const int b = ub, g = ug, r = ur;
-            ++g_next;
-            step();
-            if (n == 0) {  // an empty sequence: its group's outputs are zero
-                float *o = p.out + ((size_t)b * H_q + (size_t)g * G) * D;
-                for (int i = lane; i < G * D; i += 32) o[i] = 0.f;
-                continue;
-            }
-            pr_r = r;
-            pr_tile = 0;
-            pr_valid = min(L, n - r * L);
-            pr_ntiles = (pr_valid + T::KEYS - 1) / T::KEYS;
-            pr_grp = b * H_kv + g;
-            pr_row0 = (long long)pr_grp * p.n_max + (long long)r * L;
-        }
-        if (pr_end) {
-            if (lane == 0) desc[slot] = make_int4(DESC_END, 0, 0, 0);
-            return;
-        }
-        const int rows = min(T::KEYS, pr_valid - pr_tile * T::KEYS);
-        int flags = (pr_tile == pr_ntiles - 1) ? TF_LAST : 0;
-        uint32_t qbytes = 0;
-        if (pr_tile == 0 && pr_grp != pr_group) {
-            pr_group = pr_grp;
-            flags |= TF_NEWQ;
-            // the staging buffer is free once the consumer has started the tile that carried it
-            if (q_issue <= cons_seq) {
-                q_issue = pr_seq;
-                qbytes = T::QBYTES;
-            } else {
-                flags |= TF_QGLOBAL;
-            }
-        }
-        if (lane == 0) {
-            desc[slot] = make_int4(pr_grp, (pr_r << 8) | pr_tile, rows, flags);
-            const uint32_t bytes = (uint32_t)rows * C::ROWB;
-            const long long row = pr_row0 + (long long)pr_tile * T::KEYS;
-            uint8_t *dst = ring + slot * 2 * T::KVB;
-            mbar_arrive_tx(&bars[slot], 2 * bytes + qbytes);
-            bulk_g2s(dst, p.k + row * D, bytes, &bars[slot], policy);
-            bulk_g2s(dst + T::KVB, p.v + row * D, bytes, &bars[slot], policy);
-            if (qbytes) bulk_g2s_plain(qbuf, p.q + (size_t)pr_grp * G * D, qbytes, &bars[slot]);
-        }
-        ++pr_tile;
-        ++pr_seq;
-    };
-    for (int s = 0; s < NSTAGE; ++s) produce(s, -1);
-
-    // ---- consumer
-    unsigned long long qp[G][8];
-    float m[NV], l[NV];   // per score slot (head): running maximum (log2 units) and sum
-    float acc[G][EPL];    // this lane's output dimensions of every head
-    auto reset_unit = [&]() {
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            m[i] = NEG_INF;
-            l[i] = 0.f;
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
-    };
-    reset_unit();
-    const bool own = (sub % C::REP) == 0;
-    bool aborted = false;
-    int it = 0;
-    for (;; ++it) {
-        const int slot = it % NSTAGE;
-        __syncwarp();
-        const int4 dsc = desc[slot];
-        if (dsc.x == DESC_END) break;
-        if (!mbar_wait_bounded(&bars[slot], (uint32_t)(it / NSTAGE) & 1u, p.wait_ns)) {
-            aborted = true;
-            break;
-        }
-        const int grpid = dsc.x, ur_c = dsc.y >> 8, rows = dsc.z, flags = dsc.w;
-        if (flags & TF_NEWQ) {
-            const uint16_t *qg = (flags & TF_QGLOBAL) ? p.q + (size_t)grpid * G * D
-                                                       : reinterpret_cast<const uint16_t *>(qbuf);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const uint4 a = *reinterpret_cast<const uint4 *>(qg + h * D + 8 * sub);
-                const uint4 c = *reinterpret_cast<const uint4 *>(qg + h * D + 8 * (sub + C::P));
-                const uint32_t wv[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i) qp[h][i] = bf16x2_to_f32x2(wv[i]);
-            }
-        }
-        const uint8_t *kt = ring + slot * 2 * T::KVB;
-        const uint8_t *vt = kt + T::KVB;
-
-        // ---- scores, then the online softmax step of every head
-        float sc[NCALL][NV];
-#pragma unroll
-        for (int c = 0; c < NCALL; ++c) {
-            float val[2 * G];
-            tile_dots<D, G>(kt, c * C::KW + 2 * grp, sub, qp, val);
-#pragma unroll
-            for (int i = 0; i < NV; ++i) sc[c][i] = val[i];
-        }
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            float tm = NEG_INF;
-#pragma unroll
-            for (int c = 0; c < NCALL; ++c) {
-                const int key = c * C::KW + 2 * grp + C::key2_of(lane, i);
-                if (key < rows) tm = fmaxf(tm, __fmul_rn(sc[c][i], p.k2_hi));
-            }
-#pragma unroll
-            for (int msk = 1; msk < 32; msk <<= 1)
-                if (C::SAME & (unsigned)msk) tm = fmaxf(tm, __shfl_xor_sync(FULL, tm, msk));
-            const float mn = fmaxf(m[i], tm);
-            const float al = exp2f(m[i] - mn);  // 0 on the unit's first tile
-            const int h = C::head_of(lane, i);
-            float ps = 0.f;
-#pragma unroll
-            for (int c = 0; c < NCALL; ++c) {
-                const int key = c * C::KW + 2 * grp + C::key2_of(lane, i);
-                if (key < rows && own) {
-                    const float pv = exp2f(__fmaf_rn(sc[c][i], p.k2_lo, __fmaf_rn(sc[c][i], p.k2_hi, -mn)));
-                    pk[key * G + h] = pv;
-                    ps = __fadd_rn(ps, pv);
+                tmem_slot[1] = (uint32_t)(j + 1);
+                const int4 d = desc[s];
+                if (!mbar_wait_bounded(&tempty[a], ((uint32_t)(j / NACC) & 1u) ^ 1u, p.wait_ns)) {
+                    set_dev_error(p.ctrl, DEV_TIMEOUT);
+                    break;
                 }
-            }
-#pragma unroll
-            for (int msk = 1; msk < 32; msk <<= 1)
-                if (C::SAME & (unsigned)msk) ps = __fadd_rn(ps, __shfl_xor_sync(FULL, ps, msk));
-            l[i] = __fmaf_rn(l[i], al, ps);
-            m[i] = mn;
-            if ((lane & C::SAME) == 0 && own) alpha_s[h] = al;
-        }
-        __syncwarp();
-
-        // ---- p.V: rescale, then add the tile's rows (this lane's EPL dimensions)
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float a = alpha_s[h];
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[h][e] = __fmul_rn(acc[h][e], a);
-        }
-        auto add_row = [&](int k) {
-            float pv[G];
-            if constexpr (G % 4 == 0) {
-#pragma unroll
-                for (int h4 = 0; h4 < G; h4 += 4) {
-                    const float4 x = *reinterpret_cast<const float4 *>(pk + k * G + h4);
-                    pv[h4] = x.x;
-                    pv[h4 + 1] = x.y;
-                    pv[h4 + 2] = x.z;
-                    pv[h4 + 3] = x.w;
+                tc_fence_after();
+                adesc[a] = d;
+                if (d.x == DESC_END) {
+                    mbar_arrive(&tfull[a]);
+                    mbar_arrive(&tfull[a]);
+                    break;
                 }
-            } else {
+                const uint32_t kaddr = smem_u32(kst + s * NH * KB), qaddr = smem_u32(qst + s * NH * QB);
+                const uint32_t dt = tbase + (uint32_t)(a * UCOLS);
 #pragma unroll
-                for (int h = 0; h < G; ++h) pv[h] = pk[k * G + h];
-            }
-            float vv[EPL];
-            if constexpr (EPL == 4) {
-                const uint2 raw = *reinterpret_cast<const uint2 *>(vt + k * C::ROWB + 8 * lane);
-                vv[0] = bf16lo_to_f32(raw.x);
-                vv[1] = bf16hi_to_f32(raw.x);
-                vv[2] = bf16lo_to_f32(raw.y);
-                vv[3] = bf16hi_to_f32(raw.y);
-            } else {
-                const uint32_t raw = *reinterpret_cast<const uint32_t *>(vt + k * C::ROWB + 4 * lane);
-                vv[0] = bf16lo_to_f32(raw);
-                vv[1] = bf16hi_to_f32(raw);
-            }
+                for (int hf = 0; hf < NH; ++hf)
 #pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[h][e] = __fmaf_rn(pv[h], vv[e], acc[h][e]);
-        };
-        if (rows == T::KEYS) {  // full tiles: unrolled
-#pragma unroll
-            for (int k = 0; k < T::KEYS; ++k) add_row(k);
-        } else {
-            for (int k = 0; k < rows; ++k) add_row(k);
-        }
-        __syncwarp();
-        produce(slot, it);  // K, V and the query heads are consumed: refill the slot
-
-        // ---- end of a unit: its partial (m, l, o) per head; the last unit of a group merges
-        if (flags & TF_LAST) {
-            const size_t bh0 = (size_t)grpid * G;  // first query head of the group
-#pragma unroll
-            for (int i = 0; i < NV; ++i)
-                if ((lane & C::SAME) == 0 && own) {
-                    const size_t at = ((bh0 + C::head_of(lane, i)) * p.ns_max + ur_c) * 2;
-                    p.dpart_ml[at] = m[i];
-                    p.dpart_ml[at + 1] = l[i];
-                }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float *o = p.dpart_o + ((bh0 + h) * p.ns_max + ur_c) * D + EPL * lane;
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) o[e] = acc[h][e];
-            }
-            reset_unit();
-            __threadfence();
-            __syncwarp();
-            int done = 0;
-            if (lane == 0) done = atomicAdd(p.ctrl + CTRL_GROUPS + grpid, 1) + 1;
-            done = __shfl_sync(FULL, done, 0);
-            const int nsg = (nb[grpid / H_kv] + L - 1) / L;
-            if (done == nsg) {
-                __threadfence();
-                for (int h = 0; h < G; ++h) {
-                    const size_t base = (bh0 + h) * p.ns_max;
-                    float M = NEG_INF;
-                    for (int u = lane; u < nsg; u += 32) M = fmaxf(M, __ldcg(p.dpart_ml + (base + u) * 2));
-#pragma unroll
-                    for (int msk = 16; msk >= 1; msk >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, msk));
-                    float o[EPL], lsum = 0.f;
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) o[e] = 0.f;
-#pragma unroll 4
-                    for (int u = 0; u < nsg; ++u) {
-                        const float f = exp2f(__ldcg(p.dpart_ml + (base + u) * 2) - M);
-                        lsum = __fmaf_rn(f, __ldcg(p.dpart_ml + (base + u) * 2 + 1), lsum);
-                        const float *ou = p.dpart_o + (base + u) * D + EPL * lane;
-#pragma unroll
-                        for (int e = 0; e < EPL; ++e) o[e] = __fmaf_rn(f, __ldcg(ou + e), o[e]);
+                    for (int k = 0; k < 4; ++k) {
+                        const int t = 4 * hf + k;
+                        tc_mma_bf16(dt + (uint32_t)((t / CH) * SC_N), umma_desc_sw128(kaddr + hf * KB + k * 32),
+                                    umma_desc_sw128(qaddr + hf * QB + k * 32), IDESC, (t % CH) != 0);
                     }
-                    float *dst = p.out + (bh0 + h) * D + EPL * lane;
+                tc_commit(&tfull[a]);    // the scores are ready (the K tile has been read)
+                mbar_arrive(&tfull[a]);  // (releases adesc[a])
+            }
+            tc_commit(drain);
+            mbar_wait_bounded(drain, 0u, p.wait_ns);
+        }
+        __syncwarp();
+    } else {
+        // ================= epilogue: warp w4 owns keys 32*w4.. of every subunit (its TMEM
+        // lane quarter) and D/32 output dimensions of every head for those keys
+        const int w4 = warp;
+        float m[G], l[G], acc[G][EPL];   // running maximum (log2 units), this lane's sum, output
+        auto reset = [&]() {
 #pragma unroll
-                    for (int e = 0; e < EPL; ++e) dst[e] = __fdiv_rn(o[e], lsum);
+            for (int h = 0; h < G; ++h) {
+                m[h] = NEG_INF;
+                l[h] = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
+            }
+        };
+        reset();
+        uint32_t wg_phase = 0;
+        // rendezvous of the four epilogue warps on an mbarrier (a bounded wait, unlike bar.sync)
+        auto wg_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(wgbar);
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait_bounded(wgbar, wg_phase, p.wait_ns) ? 1 : 0;
+            __syncwarp();
+            ok = __shfl_sync(FULL, ok, 0);
+            wg_phase ^= 1u;
+            return ok != 0;
+        };
+        // this lane's output dimensions d0 .. d0+EPL-1 inside a 128-byte swizzled V row
+        const int d0 = EPL * lane;
+        const int vhalf = d0 / 64, vpiece = (d0 % 64) / 8, vbyte = (d0 % 8) * 2;
+        float *pkw = pk + w4 * 32 * G;
+        for (int j = 0;; ++j) {
+            const int a = j % NACC, s = j % NS;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait_bounded(&tfull[a], (uint32_t)(j / NACC) & 1u, p.wait_ns) ? 1 : 0;
+            __syncwarp();
+            ok = __shfl_sync(FULL, ok, 0);
+            if (!ok) {
+                if (lane == 0) set_dev_error(p.ctrl, DEV_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const int4 d = adesc[a];
+            if (d.x == DESC_END) break;
+            const int grp = d.x, r = d.y, valid = d.z, flags = d.w & 0xff;
+            const bool any = 32 * w4 < valid;  // warp-uniform
+            float sv[G];
+            if (any) {
+                float part[NP][G];
+#pragma unroll
+                for (int pp = 0; pp < NP; ++pp) {
+                    uint32_t v[G];
+                    tmem_ld32<G>(tbase + ((uint32_t)(32 * w4) << 16) + (uint32_t)(a * UCOLS + pp * SC_N), v);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) part[pp][h] = __uint_as_float(v[h]);
                 }
-                if (lane == 0) p.ctrl[CTRL_GROUPS + grpid] = 0;  // ready for the next call
+#pragma unroll
+                for (int st = 1; st < NP; st <<= 1)
+#pragma unroll
+                    for (int pp = 0; pp + st < NP; pp += 2 * st)
+#pragma unroll
+                        for (int h = 0; h < G; ++h) part[pp][h] = __fadd_rn(part[pp][h], part[pp + st][h]);
+#pragma unroll
+                for (int h = 0; h < G; ++h) sv[h] = part[0][h];
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[a]);
+            if (flags & DF_FIRST) reset();
+
+            if (any) {
+                const int key = 32 * w4 + lane;
+                const bool kv = key < valid;
+                // online softmax step per head (log2 units)
+                float tm[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) tm[h] = kv ? __fmul_rn(sv[h], p.k2_hi) : NEG_INF;
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+                    for (int h = 0; h < G; ++h) tm[h] = fmaxf(tm[h], __shfl_xor_sync(FULL, tm[h], o));
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float mn = fmaxf(m[h], tm[h]);
+                    const float al = exp2f(m[h] - mn);  // 0 on the split's first keys
+                    const float pv = kv ? exp2f(__fmaf_rn(sv[h], p.k2_lo, __fmaf_rn(sv[h], p.k2_hi, -mn))) : 0.f;
+                    l[h] = __fmaf_rn(l[h], al, pv);
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) acc[h][e] = __fmul_rn(acc[h][e], al);
+                    m[h] = mn;
+                    pkw[lane * G + h] = pv;
+                }
+                __syncwarp();
+                // p.V over this warp's keys: each lane adds its EPL dimensions of every row
+                const uint8_t *vt = vst + s * NH * KB + vhalf * KB;
+                const int nk = min(32, valid - 32 * w4);
+                auto add_row = [&](int k) {
+                    const int row = 32 * w4 + k;
+                    const uint8_t *src = vt + row * 128 + ((vpiece ^ (row & 7)) << 4) + vbyte;
+                    float vv[EPL];
+                    if constexpr (EPL == 4) {
+                        const uint2 raw2 = *reinterpret_cast<const uint2 *>(src);
+                        vv[0] = bf16lo_to_f32(raw2.x);
+                        vv[1] = bf16hi_to_f32(raw2.x);
+                        vv[2] = bf16lo_to_f32(raw2.y);
+                        vv[3] = bf16hi_to_f32(raw2.y);
+                    } else {
+                        const uint32_t raw1 = *reinterpret_cast<const uint32_t *>(src);
+                        vv[0] = bf16lo_to_f32(raw1);
+                        vv[1] = bf16hi_to_f32(raw1);
+                    }
+                    float pv[G];
+                    if constexpr (G % 4 == 0) {
+#pragma unroll
+                        for (int h4 = 0; h4 < G; h4 += 4) {
+                            const float4 x = *reinterpret_cast<const float4 *>(pkw + k * G + h4);
+                            pv[h4] = x.x;
+                            pv[h4 + 1] = x.y;
+                            pv[h4 + 2] = x.z;
+                            pv[h4 + 3] = x.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < G; ++h) pv[h] = pkw[k * G + h];
+                    }
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e) acc[h][e] = __fmaf_rn(pv[h], vv[e], acc[h][e]);
+                };
+                if (nk == 32) {
+#pragma unroll 8
+                    for (int k = 0; k < 32; ++k) add_row(k);
+                } else {
+                    for (int k = 0; k < nk; ++k) add_row(k);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage's V
+
+            if (flags & DF_LAST) {
+                // the split's partial per head: the four warps' (m, l, o) combined in fp32
+                const size_t bh0 = (size_t)grp * G;
+                bool fine = true;
+#pragma unroll
+                for (int h0 = 0; h0 < G; h0 += HR) {
+#pragma unroll
+                    for (int hh = 0; hh < HR; ++hh) {
+                        const int h = h0 + hh;
+                        float lw = l[h];
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1) lw = __fadd_rn(lw, __shfl_xor_sync(FULL, lw, o));
+                        float *cw = comb + (w4 * HR + hh) * (D + 2);
+                        if (lane == 0) {
+                            cw[0] = m[h];
+                            cw[1] = lw;
+                        }
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e) cw[2 + d0 + e] = acc[h][e];
+                    }
+                    if (!(fine = wg_sync())) break;
+                    const int t = 32 * w4 + lane;  // 0..127: one output dimension
+#pragma unroll
+                    for (int hh = 0; hh < HR; ++hh) {
+                        const int h = h0 + hh;
+                        float M = NEG_INF;
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) M = fmaxf(M, comb[(w * HR + hh) * (D + 2)]);
+                        float f[4];
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) f[w] = exp2f(comb[(w * HR + hh) * (D + 2)] - M);
+                        const size_t slot = (bh0 + h) * p.ns_max + r;
+                        if (t < D) {
+                            float o = 0.f;
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) o = __fmaf_rn(f[w], comb[(w * HR + hh) * (D + 2) + 2 + t], o);
+                            p.dpart_o[slot * D + t] = o;
+                        }
+                        if (t == 0) {
+                            float ls = 0.f;
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) ls = __fmaf_rn(f[w], comb[(w * HR + hh) * (D + 2) + 1], ls);
+                            p.dpart_ml[slot * 2] = M;
+                            p.dpart_ml[slot * 2 + 1] = ls;
+                        }
+                    }
+                    if (!(fine = wg_sync())) break;  // the buffer is free again
+                }
+                if (!fine) {
+                    if (lane == 0) set_dev_error(p.ctrl, DEV_TIMEOUT);
+                    break;
+                }
             }
         }
     }
 
-    if (aborted) {
-        // give the copies still in flight a bounded chance to land before the CTA exits
-        if (lane == 0) {
-            set_dev_error(p.ctrl, DEV_TIMEOUT);
-            for (int k = 0; k < NSTAGE; ++k) {
-                const int j = it + k;
-                if (desc[j % NSTAGE].x != DESC_END)
-                    mbar_wait_bounded(&bars[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u, p.wait_ns);
-            }
-        }
-        __syncwarp();
-    }
-    __threadfence();
+    // ---- teardown: every MMA has completed (drained above); release TMEM.  After a
+    // timeout, fills the MMA thread never consumed get a bounded wait to land first.
+    tc_fence_before();
     __syncthreads();
+    if (warp == DN_WARP_PROD && lane == 0) {
+        const int nfill = (int)tmem_slot[2];
+        for (int f = (int)tmem_slot[1]; f < nfill; ++f)
+            if (!mbar_wait_bounded(&full[f % NS], (uint32_t)(f / NS) & 1u, p.wait_ns)) break;
+    }
+    if (warp == DN_WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tbase, SC_TMEM_COLS);
+    }
+    // the merge kernel is a programmatic dependent; it waits for the whole grid
+    pdl_launch_dependents();
     if (tid == 0) {
         const int done = atomicAdd(p.ctrl + CTRL_EXIT, 1);
         if (done == (int)gridDim.x - 1) {
@@ -401,6 +507,52 @@ __global__ void __launch_bounds__(NT, 1) santa_dense_kernel(const Params p)
             p.ctrl[CTRL_EXIT] = 0;
         }
     }
+}
+
+// The log-sum-exp merge of a head's split partials: o = sum_u 2^(m_u - M) o_u / sum_u
+// 2^(m_u - M) l_u.  One CTA of D threads per (b, h_q); a head with no keys gets zeros.
+template <int D>
+__global__ void __launch_bounds__(D) santa_dense_merge_kernel(const Params p)
+{
+    __shared__ float f_s[NS_LIMIT];
+    __shared__ float red[D / 32 + 1];
+    const int bh = blockIdx.x, b = bh / p.H_q, t = threadIdx.x;
+    int n = p.seq_lens[b];
+    if (n < 0 || n > p.n_max) n = 0;  // (flagged by the main kernel)
+    const int nsg = (n + DENSE_UNIT - 1) / DENSE_UNIT;
+    pdl_wait();  // the partials are complete and visible from here on
+    if (nsg == 0) {
+        p.out[(size_t)bh * D + t] = 0.f;
+        return;
+    }
+    const float *ml = p.dpart_ml + (size_t)bh * p.ns_max * 2;
+    const float *po = p.dpart_o + (size_t)bh * p.ns_max * D;
+    float M = __int_as_float(0xff800000);
+    for (int u = t; u < nsg; u += D) {
+        const float mu = __ldcg(ml + 2 * u);
+        f_s[u] = mu;
+        M = fmaxf(M, mu);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if ((t & 31) == 0) red[t >> 5] = M;
+    __syncthreads();
+    if (t == 0) {
+        float x = red[0];
+        for (int w = 1; w < D / 32; ++w) x = fmaxf(x, red[w]);
+        red[D / 32] = x;
+    }
+    __syncthreads();
+    M = red[D / 32];
+    for (int u = t; u < nsg; u += D) f_s[u] = exp2f(f_s[u] - M);
+    __syncthreads();
+    float o = 0.f, ls = 0.f;
+#pragma unroll 16
+    for (int u = 0; u < nsg; ++u) {
+        o = __fmaf_rn(f_s[u], __ldcg(po + (size_t)u * D + t), o);
+        ls = __fmaf_rn(f_s[u], __ldcg(ml + 2 * u + 1), ls);
+    }
+    p.out[(size_t)bh * D + t] = __fdiv_rn(o, ls);
 }
 
 }  // namespace santa

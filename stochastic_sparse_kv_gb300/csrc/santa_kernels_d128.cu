@@ -17,6 +17,7 @@ const void *kernel_d128(int kind, int G)
         }
         return nullptr;
     }
+    if (kind == KIND_DMERGE) return (const void *)santa_dense_merge_kernel<128>;
     if (kind == KIND_SCORE) {
         switch (G) {
         case 1: return (const void *)santa_score_kernel<128, 1>;

@@ -17,6 +17,7 @@ const void *kernel_d64(int kind, int G)
         }
         return nullptr;
     }
+    if (kind == KIND_DMERGE) return (const void *)santa_dense_merge_kernel<64>;
     if (kind == KIND_SCORE) {
         switch (G) {
         case 1: return (const void *)santa_score_kernel<64, 1>;

@@ -87,9 +87,9 @@ __host__ __device__ inline ScoreSmem score_smem(int D, int B)
     return s;
 }
 
-// The work-item space of the sampled path, built by one warp: nb[b] (checked lengths)
-// and prefix[0..B] of the unit counts H_kv * ceil(n_b / SC_M) (H_kv for n_b = 0).
-__device__ __forceinline__ void score_item_space(const Params &p, int *nb, int *prefix)
+// A kernel's work-item space, built by one warp: nb[b] (checked lengths) and
+// prefix[0..B] of the unit counts H_kv * ceil(n_b / L) (H_kv for n_b = 0).
+__device__ __forceinline__ void warp_item_space(const Params &p, int L, int *nb, int *prefix)
 {
     constexpr int PER = BMAX / 32;
     const int lane = threadIdx.x & 31;
@@ -105,7 +105,7 @@ __device__ __forceinline__ void score_item_space(const Params &p, int *nb, int *
                 n = 0;
             }
             nb[b] = n;
-            sum += p.H_kv * (n > 0 ? (n + SC_M - 1) / SC_M : 1);
+            sum += p.H_kv * (n > 0 ? (n + L - 1) / L : 1);
         }
     }
     int x = sum;
@@ -119,7 +119,7 @@ __device__ __forceinline__ void score_item_space(const Params &p, int *nb, int *
         const int b = lane * PER + i;
         if (b < p.B) {
             prefix[b] = run;
-            run += p.H_kv * (nb[b] > 0 ? (nb[b] + SC_M - 1) / SC_M : 1);
+            run += p.H_kv * (nb[b] > 0 ? (nb[b] + L - 1) / L : 1);
         }
     }
     if (lane == 31) prefix[p.B] = x;
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(SC_NT, 1)
             mbar_init(drain, 1);
             mbar_fence_init();
         }
-        score_item_space(p, nb, prefix);
+        warp_item_space(p, SC_M, nb, prefix);
     }
     // rows G..SC_N-1 of every query tile: zero (the TMA copies fill rows 0..G-1)
     {
