@@ -283,7 +283,19 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     int dev, sms, optin;
     if ((rc = device_info(&dev, &sms, &optin))) return rc;
     const int D = shape->d, G = shape->H_q / shape->H_kv;
-    const int L = dense ? DENSE_UNIT : SC_M;  // keys per work unit
+    // keys per work unit: SC_M (sampled); DENSE_UNIT times 4, 2 or 1 (dense), the largest
+    // that still leaves every SM a dozen splits (fewer partials for the merge to read)
+    int L = SC_M;
+    if (dense) {
+        L = DENSE_UNIT;
+        for (int f = 4; f > 1; f /= 2) {
+            const int Lf = DENSE_UNIT * f;
+            if ((long long)shape->B * shape->H_kv * ((shape->n_max + Lf - 1) / Lf) >= 12LL * sms) {
+                L = Lf;
+                break;
+            }
+        }
+    }
     // the kernels address K and V rows with 32-bit TMA coordinates
     if ((long long)shape->B * shape->H_kv * shape->n_max >= (1ll << 31)) return SANTA_ERR_UNSUPPORTED;
 
@@ -367,7 +379,7 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
         if (!fm) return SANTA_ERR_UNSUPPORTED;
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3((unsigned)(shape->B * shape->H_q));
-        cfg.blockDim = dim3((unsigned)D);
+        cfg.blockDim = dim3((unsigned)(MG_SLICES * D));
         cfg.dynamicSmemBytes = 0;
         cfg.stream = (cudaStream_t)stream;
         cudaLaunchAttribute attr[1];

@@ -12,7 +12,8 @@
 //    cores: the scores' online softmax per head, and p.V with V read from the stage
 //    (each lane owns D/32 output dimensions of every head, p broadcast through shared
 //    memory);
-//  * the work items are splits of DENSE_UNIT keys (a static contiguous block per CTA,
+//  * the work items are splits of p.L keys (DENSE_UNIT, or 2 or 4 times that when the
+//    problem has enough splits to keep every SM busy; a static contiguous block per CTA,
 //    then shrinking grabs); the four warps combine their running (m, l, o) at the end of
 //    a split and write one partial per (head, split);
 //  * santa_dense_merge_kernel, a programmatic dependent launch, combines a head's
@@ -76,13 +77,12 @@ __global__ void __launch_bounds__(DN_NT, 1)
     constexpr int UCOLS = score_ucols(D);
     constexpr int NACC = score_nacc(D);
     constexpr int EPL = D / 32;              // output dimensions per lane
-    constexpr int L = DENSE_UNIT;            // keys per split (one partial)
+    const int L = p.L;                       // keys per split (one partial), a multiple of SC_M
     constexpr int HR = G < DN_HROUND ? G : DN_HROUND;
     constexpr uint32_t IDESC = idesc_bf16_f32(SC_M, SC_N);
     constexpr unsigned FULL = 0xffffffffu;
     static_assert(G >= 1 && G <= 8 && SC_N >= G, "query heads per group");
     static_assert(NS >= 2 && NACC >= 2, "stage ring and accumulators");
-    static_assert(L % SC_M == 0, "a split is whole subunits");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -510,25 +510,32 @@ __global__ void __launch_bounds__(DN_NT, 1)
 }
 
 // The log-sum-exp merge of a head's split partials: o = sum_u 2^(m_u - M) o_u / sum_u
-// 2^(m_u - M) l_u.  One CTA of D threads per (b, h_q); a head with no keys gets zeros.
+// 2^(m_u - M) l_u.  One CTA of MG_SLICES * D threads per (b, h_q): slice k adds the splits
+// u = k mod MG_SLICES, and the slices' sums are added in slice order.  A head with no keys
+// gets zeros.
+constexpr int MG_SLICES = 4;
+
 template <int D>
-__global__ void __launch_bounds__(D) santa_dense_merge_kernel(const Params p)
+__global__ void __launch_bounds__(MG_SLICES * D) santa_dense_merge_kernel(const Params p)
 {
+    constexpr int NTM = MG_SLICES * D;
     __shared__ float f_s[NS_LIMIT];
-    __shared__ float red[D / 32 + 1];
+    __shared__ float red[NTM / 32 + 1];
+    __shared__ float part[MG_SLICES][D + 1];
     const int bh = blockIdx.x, b = bh / p.H_q, t = threadIdx.x;
+    const int dim = t % D, slice = t / D;
     int n = p.seq_lens[b];
     if (n < 0 || n > p.n_max) n = 0;  // (flagged by the main kernel)
-    const int nsg = (n + DENSE_UNIT - 1) / DENSE_UNIT;
+    const int nsg = (n + p.L - 1) / p.L;
     pdl_wait();  // the partials are complete and visible from here on
     if (nsg == 0) {
-        p.out[(size_t)bh * D + t] = 0.f;
+        if (t < D) p.out[(size_t)bh * D + t] = 0.f;
         return;
     }
     const float *ml = p.dpart_ml + (size_t)bh * p.ns_max * 2;
     const float *po = p.dpart_o + (size_t)bh * p.ns_max * D;
     float M = __int_as_float(0xff800000);
-    for (int u = t; u < nsg; u += D) {
+    for (int u = t; u < nsg; u += NTM) {
         const float mu = __ldcg(ml + 2 * u);
         f_s[u] = mu;
         M = fmaxf(M, mu);
@@ -539,20 +546,31 @@ __global__ void __launch_bounds__(D) santa_dense_merge_kernel(const Params p)
     __syncthreads();
     if (t == 0) {
         float x = red[0];
-        for (int w = 1; w < D / 32; ++w) x = fmaxf(x, red[w]);
-        red[D / 32] = x;
+        for (int w = 1; w < NTM / 32; ++w) x = fmaxf(x, red[w]);
+        red[NTM / 32] = x;
     }
     __syncthreads();
-    M = red[D / 32];
-    for (int u = t; u < nsg; u += D) f_s[u] = exp2f(f_s[u] - M);
+    M = red[NTM / 32];
+    for (int u = t; u < nsg; u += NTM) f_s[u] = exp2f(f_s[u] - M);
     __syncthreads();
     float o = 0.f, ls = 0.f;
-#pragma unroll 16
-    for (int u = 0; u < nsg; ++u) {
-        o = __fmaf_rn(f_s[u], __ldcg(po + (size_t)u * D + t), o);
+#pragma unroll 8
+    for (int u = slice; u < nsg; u += MG_SLICES) {
+        o = __fmaf_rn(f_s[u], __ldcg(po + (size_t)u * D + dim), o);
         ls = __fmaf_rn(f_s[u], __ldcg(ml + 2 * u + 1), ls);
     }
-    p.out[(size_t)bh * D + t] = __fdiv_rn(o, ls);
+    part[slice][dim] = o;
+    if (dim == 0) part[slice][D] = ls;
+    __syncthreads();
+    if (t < D) {
+        float os = 0.f, lt = 0.f;
+#pragma unroll
+        for (int k = 0; k < MG_SLICES; ++k) {
+            os = __fadd_rn(os, part[k][t]);
+            lt = __fadd_rn(lt, part[k][D]);
+        }
+        p.out[(size_t)bh * D + t] = __fdiv_rn(os, lt);
+    }
 }
 
 }  // namespace santa
