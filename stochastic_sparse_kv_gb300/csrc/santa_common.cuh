@@ -16,14 +16,12 @@ namespace santa {
 
 constexpr int NT = 256;              // threads per CTA
 constexpr int NWARP = NT / 32;       // 8 warps
-constexpr int LMIN = 128;            // (tile-size check of the score helpers)
 constexpr int DENSE_UNIT = 512;      // keys per work unit (and per partial) of the dense kernel
 constexpr int CHUNK = 32;            // keys per CDF chunk (one 128-byte line of fp32 w)
 constexpr int NS_LIMIT = 1024;       // most dense splits one sequence may have
 constexpr int NMAX_LIMIT = 524288;   // longest KV cache (keys)
 constexpr int BMAX = 1024;           // batch rows per call
 constexpr int SMAX = 4096;           // samples per (b, h)
-constexpr int TILE_BYTES = 16384;    // one staged K (or V) tile
 
 // Control block (int32 words at the start of the workspace).
 enum : int { CTRL_ERR = 0, CTRL_WORK = 1, CTRL_EXIT = 2, CTRL_GROUPS = 64 };
@@ -172,27 +170,6 @@ __device__ __forceinline__ void st_hint(int *a, int v, uint64_t pol)
     asm volatile("st.global.L2::cache_hint.s32 [%0], %1, %2;" ::"l"(a), "r"(v), "l"(pol) : "memory");
 }
 
-// 1-D bulk copy global -> shared (TMA engine), completion counted on `bar` in bytes.
-// dst, src 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                         uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
-// The same without an L2 eviction hint (data other warps re-read).
-__device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
 // Drop the 128-byte L2 lines lying wholly inside [base, base + bytes) without writing
 // them back: their data becomes undefined.  For scratch that has been read for the last
 // time, so that dirty lines are not evicted to DRAM later.  Threads tid of nt share it.
@@ -213,50 +190,9 @@ __device__ __forceinline__ void prefetch_l2(const void *p)
 
 // ------------------------------------------------------------------ arithmetic
 
-// bf16 pair (low element in the low half) -> packed fp32 pair, exact.
-__device__ __forceinline__ unsigned long long bf16x2_to_f32x2(uint32_t w)
-{
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xffff0000u));
-    return r;
-}
-
+// bf16 halves of a 32-bit word -> fp32, exact.
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// acc += a * b on two fp32 lanes at once (Blackwell packed FMA).
-__device__ __forceinline__ void ffma2(unsigned long long &acc, unsigned long long a, unsigned long long b)
-{
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
-}
-
-__device__ __forceinline__ unsigned long long fmul2(unsigned long long a, unsigned long long b)
-{
-    unsigned long long r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-
-__device__ __forceinline__ float f32x2_sum(unsigned long long x)
-{
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
-    return __fadd_rn(lo, hi);
-}
-
-__device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi)
-{
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
-__device__ __forceinline__ float2 f32x2_unpack(unsigned long long x)
-{
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
-    return make_float2(lo, hi);
-}
 
 // Error-free transformations (Knuth's TwoSum, Dekker's Fast2Sum, FMA-based TwoProd):
 // s + e == a + b exactly.  The _rn intrinsics keep the compiler from contracting or
@@ -385,9 +321,6 @@ __device__ __forceinline__ int fkey(float x)
     return i >= 0 ? i : (i ^ 0x7fffffff);
 }
 __device__ __forceinline__ float fkey_inv(int k) { return __int_as_float(k >= 0 ? k : (k ^ 0x7fffffff)); }
-
-// Non-negative fp64 values compare like their bit patterns as unsigned integers.
-__device__ __forceinline__ uint64_t dkey(double x) { return (uint64_t)__double_as_longlong(x); }
 
 __device__ __forceinline__ void set_dev_error(int32_t *ctrl, int bits)
 {

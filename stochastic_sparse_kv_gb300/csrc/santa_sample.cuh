@@ -5,51 +5,13 @@
 // S << n_k indices from it (stratified or systematic sampling) and gather-adds only
 // those V rows, scaled by 1/S.  The score stage is santa_score_kernel
 // (santa_score.cuh), the value stage santa_gather_kernel (santa_gather.cuh); this file
-// holds the pieces they and the dense kernel share: the per-tile grouped-query dot
-// products, the error-free re-scoring of heavy keys, the work-item space and small
-// block-level helpers.
+// holds the pieces they and the dense kernel share: the work-item space, the error-free
+// re-scoring of heavy keys and small block-level helpers.
 #pragma once
 
 #include "santa_common.cuh"
 
 namespace santa {
-
-template <int D, int G>
-struct SampleCfg {
-    static constexpr int P = D / 16;            // lanes per key in the score loop
-    static constexpr int KW = 64 / P;           // keys per warp and tile (2 per lane group)
-    static constexpr int TK = NWARP * KW;       // keys per tile
-    static constexpr int ROWB = 2 * D;          // bytes per K row
-    static constexpr int NSTAGE = 4;
-    static constexpr int V = 2 * G;             // partial dots per lane
-    static constexpr int NV = V >= P ? V / P : 1;   // scores per lane after the reduction
-    static constexpr int REP = V >= P ? 1 : P / V;  // lanes holding the same score
-    static constexpr int EPL = D / 32;          // V elements per lane in the gather
-    static_assert(TK * ROWB == TILE_BYTES, "tile size");
-    static_assert(LMIN % TK == 0, "split length must be a multiple of the tile");
-
-    __host__ __device__ static constexpr int vidx(int sub, int i) { return V >= P ? sub * NV + i : sub / REP; }
-    __host__ __device__ static constexpr int head_of(int lane, int i) { return vidx(lane % P, i) % G; }
-    __host__ __device__ static constexpr int key2_of(int lane, int i) { return vidx(lane % P, i) / G; }
-    // Flipping lane bit m leaves the heads of every score slot unchanged.
-    __host__ __device__ static constexpr bool same_heads(int m)
-    {
-        for (int l = 0; l < 32; ++l)
-            for (int i = 0; i < NV; ++i)
-                if (head_of(l ^ m, i) != head_of(l, i)) return false;
-        return true;
-    }
-    __host__ __device__ static constexpr unsigned same_mask()
-    {
-        unsigned r = 0;
-        for (int m = 1; m < 32; m <<= 1)
-            if (same_heads(m)) r |= (unsigned)m;
-        return r;
-    }
-    // Lane-xor masks (as a bit set) that keep every score slot's head: evaluated by the
-    // compiler, so the per-tile reductions below unroll to a fixed shuffle sequence.
-    static constexpr unsigned SAME = same_mask();
-};
 
 __host__ __device__ inline int next_pow2(int x)
 {
@@ -58,12 +20,8 @@ __host__ __device__ inline int next_pow2(int x)
     return p;
 }
 
-// Descriptor of a staged tile (int4: group b*H_kv+g, (unit << 8) | tile, rows, flags).
+// Marker of the end of the work in a staged-tile descriptor (int4; x = DESC_END).
 enum : int { DESC_END = -1 };
-// Flags: the tile is the first of a new (b, g), whose query heads come in staging buffer
-// (flags >> TF_QB_SHIFT) & 1, or must be read from global memory; the tile is the last
-// of its work unit.
-enum : int { TF_NEWQ = 1, TF_QGLOBAL = 2, TF_QB_SHIFT = 2, TF_LAST = 8 };
 
 struct Item {
     int b, g, r, n, ns;
@@ -85,61 +43,6 @@ __device__ __forceinline__ Item decode_item(int it, const int *prefix, const int
     x.r = local % x.ns;
     (void)H_kv;
     return x;
-}
-
-// Reduce-scatter of the V partial dots of a lane group of P lanes: after it the lane
-// keeps the sums of the value slots given by SampleCfg::vidx.
-template <int M, int C, int V>
-__device__ __forceinline__ void rs_step(float (&val)[V], int sub)
-{
-    if constexpr (M >= 1) {
-        if constexpr (C > 1) {
-            constexpr int H = C / 2;
-            const bool up = (sub & M) != 0;
-#pragma unroll
-            for (int i = 0; i < H; ++i) {
-                const float send = up ? val[i] : val[i + H];
-                const float recv = __shfl_xor_sync(0xffffffffu, send, M);
-                val[i] = __fadd_rn(up ? val[i + H] : val[i], recv);
-            }
-            rs_step<M / 2, H, V>(val, sub);
-        } else {
-            val[0] = __fadd_rn(val[0], __shfl_xor_sync(0xffffffffu, val[0], M));
-            rs_step<M / 2, 1, V>(val, sub);
-        }
-    }
-}
-
-// fp32 dots of 2 keys (rows kbase, kbase+1 of the tile) with the G query heads; lane
-// sub of the group holds 16 elements: 16-byte chunks sub and sub + P of each row.
-template <int D, int G>
-__device__ __forceinline__ void tile_dots(const uint8_t *tile, int kbase, int sub,
-                                          const unsigned long long (&qp)[G][8], float (&val)[2 * G])
-{
-    using C = SampleCfg<D, G>;
-    unsigned long long acc[2][G];
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-        for (int h = 0; h < G; ++h) acc[kk][h] = 0ull;
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-        const uint8_t *row = tile + (kbase + kk) * C::ROWB;
-        const uint4 a = *reinterpret_cast<const uint4 *>(row + 16 * sub);
-        const uint4 c = *reinterpret_cast<const uint4 *>(row + 16 * (sub + C::P));
-        const uint32_t wv[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const unsigned long long kp = bf16x2_to_f32x2(wv[i]);
-#pragma unroll
-            for (int h = 0; h < G; ++h) ffma2(acc[kk][h], qp[h][i], kp);
-        }
-    }
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-        for (int h = 0; h < G; ++h) val[kk * G + h] = f32x2_sum(acc[kk][h]);
-    rs_step<C::P / 2, 2 * G, 2 * G>(val, sub);
 }
 
 // Error-free score of one K row (global memory) with query head qf (fp32 copies of the
@@ -240,49 +143,6 @@ __device__ __forceinline__ int upper_bound_i(const int *a, int n, int key)
     }
     return lo;
 }
-
-
-
-// misc[] words of a kernel's shared block
-enum : int { MISC_SCAN = 0 /* NWARP+1 words */, MISC_LAST = 12 };
-
-// Work items of a call: per batch row b, H_kv * ceil(n_b / L) splits (H_kv items when
-// n_b = 0).  Fills nb[b] (clamped lengths) and the exclusive prefix prefix[0..B] of the
-// item counts; flags out-of-range lengths.  Called by every thread of the CTA.
-__device__ __forceinline__ void build_item_space(const Params &p, int *nb, int *prefix, int *misc)
-{
-    constexpr int PER = (BMAX + NT - 1) / NT;
-    const int tid = threadIdx.x;
-    int cnt[PER];
-    int local = 0;
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int b = tid * PER + i;
-        cnt[i] = 0;
-        if (b < p.B) {
-            int n = p.seq_lens[b];
-            if (n < 0 || n > p.n_max) {
-                bad = true;
-                n = 0;
-            }
-            nb[b] = n;
-            cnt[i] = p.H_kv * (n > 0 ? (n + p.L - 1) / p.L : 1);
-            local += cnt[i];
-        }
-    }
-    if (bad && blockIdx.x == 0) set_dev_error(p.ctrl, DEV_BAD_SEQLEN);
-    int total;
-    int run = block_excl_scan(local, misc + MISC_SCAN, &total);
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int b = tid * PER + i;
-        if (b < p.B) prefix[b] = run;
-        run += cnt[i];
-    }
-    if (tid == 0) prefix[p.B] = total;
-}
-
 __device__ __forceinline__ void pdl_launch_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
