@@ -184,6 +184,66 @@ def max_over_ranks(value, dist=None, device="cpu"):
     return float(t.item())
 
 
+def multi_layer(n_layers, w, S, dev, peak, reps=20):
+    """Attention of one decode step through an n_layers-deep model without weights: every
+    layer has its own KV cache (so nothing is reused from L2 between layers) and writes a
+    bf16 output, and the whole stack of calls is captured in one CUDA graph and replayed.
+    Returns per-token times for the sampled (systematic) and the dense path."""
+    import torch
+    from stochastic_sparse_kv_gb300 import santa
+    B, H_q, H_kv, d, n = w.B, w.H_q, w.H_kv, w.d, w.n_max
+    try:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(20261202)
+        kv, qs = [], []
+        for _ in range(n_layers):
+            kv.append((torch.randn(B, H_kv, n, d, device=dev, generator=gen).to(torch.bfloat16),
+                       torch.randn(B, H_kv, n, d, device=dev, generator=gen).to(torch.bfloat16)))
+            g = torch.randn(B, H_q, d, device=dev, generator=gen)
+            qs.append((3.0 * d ** 0.5 * g / g.norm(dim=-1, keepdim=True)).to(torch.bfloat16))
+    except torch.cuda.OutOfMemoryError as e:
+        return {"skipped": f"out of device memory for {n_layers} layers: {e}"[:200]}
+    sl = torch.full((B,), n, dtype=torch.int32, device=dev)
+    outs = [torch.empty(B, H_q, d, dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
+    shape = santa.make_shape(B, H_q, H_kv, d, n)
+    ws = santa.new_workspace(max(santa.workspace_size(shape, S, "systematic"),
+                                 santa.workspace_size(shape, 1, "dense")), dev)
+    res = {"layers": n_layers, "kv_cache_gb": round(n_layers * 2 * B * H_kv * n * d * 2 / 1e9, 1),
+           "out": "bf16", "graph": True}
+    for mode in ("systematic", "dense"):
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for li in range(n_layers):  # eager warm-up (kernel attributes, tensor maps)
+                santa.decode(qs[li], kv[li][0], kv[li][1], sl, S, mode, seed=li, out=outs[li], want_idx=False,
+                             workspace=ws, stream=side)
+        side.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for li in range(n_layers):
+                    santa.decode(qs[li], kv[li][0], kv[li][1], sl, S, mode, seed=li, out=outs[li],
+                                 want_idx=False, workspace=ws, stream=side)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us_tok = e0.elapsed_time(e1) * 1000.0 / reps
+        ab = n_layers * algorithmic_bytes(B, H_q, H_kv, d, [n] * B, S, mode)
+        res[mode] = {"us_per_token": round(us_tok, 1), "us_per_layer": round(us_tok / n_layers, 2),
+                     "frac_of_peak": round(ab / (us_tok * 1e-6) / 1e9 / peak, 4)}
+        del graph
+    res["speedup_vs_dense"] = round(res["dense"]["us_per_token"] / res["systematic"]["us_per_token"], 3)
+    del kv, qs, outs
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -253,6 +313,12 @@ def run_ours(args):
             row["group_dedup" if flag else "per_head"] = round(tm * 1000 / extra_steps, 2)
         gdd[str(S2)] = row
 
+    # the attention of a whole decode step through a 32-layer stack (CUDA graph, bf16 out)
+    ml = None
+    if not args.no_extras and args.layers > 0 and world == 1:
+        log(f"[bench] multi-layer decode: {args.layers} layers ...")
+        ml = multi_layer(args.layers, w, S, dev, peak)
+
     # end to end through the C ABI with host buffers: H2D inputs, decode, D2H result
     e2e = None
     if args.e2e_steps > 0:
@@ -302,6 +368,7 @@ def run_ours(args):
             "modes": modes,
             "S_sweep_systematic": sweep,
             "group_dedup_us_per_step": gdd,
+            "multi_layer": ml,
         }
         print(json.dumps(rec), flush=True)
     if dist is not None:
@@ -383,6 +450,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the other modes and the S sweep")
     ap.add_argument("--workload", default="llama8b_b16_32k")
+    ap.add_argument("--layers", type=int, default=32, help="depth of the multi-layer extra (0: skip it)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -58,6 +58,12 @@ extern "C" {
  * to fp32 rounding of the sums. */
 #define SANTA_GROUP_DEDUP 0x100
 
+/* Flag, or-ed into any mode: write `out` as bf16 [B, H_q, d] instead of fp32 (the caller
+ * passes a bf16 buffer through the float* parameter).  Each element is the fp32 result
+ * rounded once to the nearest bf16 (ties to even), so it equals the fp32 output rounded.
+ * For a caller whose next layer consumes bf16 activations. */
+#define SANTA_OUT_BF16 0x200
+
 /* Device error bits (santa_device_status). */
 #define SANTA_DEV_BAD_SEQLEN 1      /* some seq_lens[b] outside [0, n_max]; treated as 0 */
 #define SANTA_DEV_TIMEOUT 2         /* a bounded wait on a shared-memory barrier gave up */
@@ -96,9 +102,9 @@ int santa_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
  *            and set SANTA_DEV_BAD_SEQLEN in the device error word
  *  S         samples per (b, h): 1..4096 (ignored for SANTA_DENSE)
  *  mode      SANTA_DENSE, SANTA_STRATIFIED, SANTA_SYSTEMATIC or SANTA_IID, optionally
- *            or-ed with SANTA_GROUP_DEDUP
+ *            or-ed with SANTA_GROUP_DEDUP and SANTA_OUT_BF16
  *  seed      Philox4x64-10 key word 0 (ignored for SANTA_DENSE)
- *  out       device fp32 [B, H_q, d]; n_b = 0 gives zeros
+ *  out       device fp32 [B, H_q, d] (bf16 with SANTA_OUT_BF16); n_b = 0 gives zeros
  *  idx_out   device int32 [B, H_q, S] or NULL: the sampled key indices of each (b, h),
  *            ascending, with repeats; n_b = 0 gives -1 (ignored for SANTA_DENSE)
  *  workspace device buffer of at least santa_workspace_size bytes, 256-byte aligned,

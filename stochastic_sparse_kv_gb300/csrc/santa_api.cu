@@ -168,7 +168,7 @@ int check_shape(const santa_shape *sh)
 
 int check_mode_S(int32_t mode_flags, int32_t S)
 {
-    if (mode_flags & ~(0xff | SANTA_GROUP_DEDUP)) return SANTA_ERR_INVALID_ARG;
+    if (mode_flags & ~(0xff | SANTA_GROUP_DEDUP | SANTA_OUT_BF16)) return SANTA_ERR_INVALID_ARG;
     const int mode = mode_flags & 0xff;
     if (mode < SANTA_DENSE || mode > SANTA_IID) return SANTA_ERR_INVALID_ARG;
     if (mode != SANTA_DENSE && (S < 1 || S > SMAX)) return SANTA_ERR_INVALID_ARG;
@@ -328,6 +328,7 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     p.L = L;
     p.S = dense ? 1 : S;
     p.mode = mode;
+    p.out_bf16 = (mode_flags & SANTA_OUT_BF16) ? 1 : 0;
     p.seed = seed;
     p.rS = 1.0 / (double)p.S;
     const float scale = shape->scale != 0.f ? shape->scale : (float)(1.0 / std::sqrt((double)D));

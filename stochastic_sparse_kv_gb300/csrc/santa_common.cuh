@@ -10,6 +10,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace santa {
@@ -80,12 +81,22 @@ struct Params {
     int L;            // keys per work unit (sampled path) or split length (dense), multiple of 64
     int S, mode;
     int xdedup;       // value stage: the group's heads share V loads (thread-block clusters)
+    int out_bf16;     // out is bf16 (each fp32 result rounded once), else fp32
     uint64_t seed;
     double rS;        // fp64 value nearest 1/S
     float k2_hi, k2_lo;  // scale*log2(e) as an unevaluated fp32 sum
     float tau2;       // re-scoring window below the maximum (log2 units)
     uint64_t wait_ns; // bounded-wait limit
 };
+
+// out[i] = v, as fp32 or rounded once to bf16 (round to nearest, ties to even).
+__device__ __forceinline__ void store_out(const Params &p, size_t i, float v)
+{
+    if (p.out_bf16)
+        reinterpret_cast<__nv_bfloat16 *>(p.out)[i] = __float2bfloat16_rn(v);
+    else
+        p.out[i] = v;
+}
 
 // ------------------------------------------------------------------ PTX wrappers
 

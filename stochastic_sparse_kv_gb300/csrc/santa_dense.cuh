@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(MG_SLICES * D) santa_dense_merge_kernel(const 
     const int nsg = (n + p.L - 1) / p.L;
     pdl_wait();  // the partials are complete and visible from here on
     if (nsg == 0) {
-        if (t < D) p.out[(size_t)bh * D + t] = 0.f;
+        if (t < D) store_out(p, (size_t)bh * D + t, 0.f);
         return;
     }
     const float *ml = p.dpart_ml + (size_t)bh * p.ns_max * 2;
@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(MG_SLICES * D) santa_dense_merge_kernel(const 
             os = __fadd_rn(os, part[k][t]);
             lt = __fadd_rn(lt, part[k][D]);
         }
-        p.out[(size_t)bh * D + t] = __fdiv_rn(os, lt);
+        store_out(p, (size_t)bh * D + t, __fdiv_rn(os, lt));
     }
 }
 

@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
     int n = p.seq_lens[b];
     if (n < 0 || n > p.n_max) n = 0;  // flagged by the score kernel
     if (n == 0) {
-        for (int i = tid; i < D; i += NT) p.out[(size_t)bh * D + i] = 0.f;
+        for (int i = tid; i < D; i += NT) store_out(p, (size_t)bh * D + i, 0.f);
         if (p.idx_out)
             for (int i = tid; i < S; i += NT) p.idx_out[(size_t)bh * S + i] = -1;
         return;
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
                 float sum = 0.f;
 #pragma unroll
                 for (int jj = 0; jj < G; ++jj) sum = __fadd_rn(sum, recv[jj * D + i]);
-                p.out[(size_t)bh * D + i] = __fdiv_rn(sum, (float)S);
+                store_out(p, (size_t)bh * D + i, __fdiv_rn(sum, (float)S));
             }
             return;
         }
@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
         for (int i = tid; i < D; i += NT) {
             float sum = 0.f;
             for (int r = 0; r < RSTEP; ++r) sum = __fadd_rn(sum, acc_s[(r * NPC + i / 8) * 8 + i % 8]);
-            p.out[(size_t)bh * D + i] = __fdiv_rn(sum, (float)S);
+            store_out(p, (size_t)bh * D + i, __fdiv_rn(sum, (float)S));
         }
     }
 }

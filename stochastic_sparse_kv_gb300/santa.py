@@ -19,6 +19,7 @@ OK = 0
 DENSE, STRATIFIED, SYSTEMATIC, IID = 0, 1, 2, 3
 MODES = {"dense": DENSE, "stratified": STRATIFIED, "systematic": SYSTEMATIC, "iid": IID}
 GROUP_DEDUP = 0x100  # or-ed into a sampling mode: V rows loaded once per KV-head group
+OUT_BF16 = 0x200     # or-ed into any mode: out is bf16 (the fp32 result rounded once)
 DEV_BAD_SEQLEN, DEV_TIMEOUT = 1, 2
 
 # every symbol include/santa.h declares
@@ -128,10 +129,11 @@ def _cached_workspace(nbytes: int, device, stream) -> torch.Tensor:
 def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens: torch.Tensor,
            S: int, mode="systematic", seed: int = 0, scale: float = 0.0, out: torch.Tensor | None = None,
            idx_out: torch.Tensor | None = None, want_idx: bool = True, workspace: torch.Tensor | None = None,
-           stream=None, group_dedup: bool = False):
+           stream=None, group_dedup: bool = False, out_dtype: torch.dtype = torch.float32):
     """One SANTA (or dense) decode step on the GPU.  q [B,H_q,d], k/v [B,H_kv,n_max,d] bf16,
-    seq_lens [B] int32, all on one CUDA device.  Returns (out fp32 [B,H_q,d],
-    idx int32 [B,H_q,S] or None).  group_dedup: load each sampled V row once per group of
+    seq_lens [B] int32, all on one CUDA device.  Returns (out [B,H_q,d], idx int32
+    [B,H_q,S] or None).  out is fp32, or bf16 (SANTA_OUT_BF16) when `out` is a bf16 tensor
+    or out_dtype is torch.bfloat16.  group_dedup: load each sampled V row once per group of
     query heads sharing a KV head (SANTA_GROUP_DEDUP)."""
     m = _mode(mode)
     B, H_q, d = q.shape
@@ -146,12 +148,14 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_le
     shape = make_shape(B, H_q, H_kv, d, n_max, scale)
     dev = q.device
     if out is None:
-        out = torch.empty(B, H_q, d, dtype=torch.float32, device=dev)
+        out = torch.empty(B, H_q, d, dtype=out_dtype, device=dev)
+    if out.dtype not in (torch.float32, torch.bfloat16) or not out.is_contiguous() or out.shape != (B, H_q, d):
+        raise ValueError("out must be a contiguous fp32 or bf16 [B, H_q, d] tensor")
     if m != DENSE and want_idx and idx_out is None:
         idx_out = torch.empty(B, H_q, S, dtype=torch.int32, device=dev)
     nbytes = workspace_size(shape, S if m != DENSE else 1, m)
     ws = workspace if workspace is not None else _cached_workspace(nbytes, dev, stream)
-    mf = m | (GROUP_DEDUP if (group_dedup and m != DENSE) else 0)
+    mf = m | (GROUP_DEDUP if (group_dedup and m != DENSE) else 0) | (OUT_BF16 if out.dtype == torch.bfloat16 else 0)
     rc = load().santa_decode(ctypes.byref(shape), ctypes.c_void_p(q.data_ptr()),
                              ctypes.c_void_p(k_cache.data_ptr()), ctypes.c_void_p(v_cache.data_ptr()),
                              ctypes.c_void_p(seq_lens.data_ptr()), int(S), mf, ctypes.c_uint64(seed),

@@ -60,7 +60,9 @@ def test_workspace_size_matches_layout(lib):
     ((1, 32, 8, 128, 1024), 0, 0, 0),           # dense ignores S
     ((1, 32, 8, 128, 1024), 16, 7, -1),         # bad mode
     ((1, 32, 8, 128, 1024), 16, 0x102, 0),      # SANTA_GROUP_DEDUP is a valid flag
-    ((1, 32, 8, 128, 1024), 16, 0x202, -1),     # unknown flag bits
+    ((1, 32, 8, 128, 1024), 16, 0x202, 0),      # SANTA_OUT_BF16 is a valid flag
+    ((1, 32, 8, 128, 1024), 16, 0x302, 0),      # both flags
+    ((1, 32, 8, 128, 1024), 16, 0x402, -1),     # unknown flag bits
     ((1025, 32, 8, 128, 1024), 16, 2, -4),      # B > 1024
     ((1, 32, 8, 128, 524289), 16, 2, -4),       # n_max too large
 ])

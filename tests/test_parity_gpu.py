@@ -141,6 +141,51 @@ def test_small_dense(d, H_q, H_kv, n_max, seq, S):
             assert np.all(out.numpy()[b] == 0)
 
 
+@pytest.mark.parametrize("mode,dedup", [("systematic", False), ("stratified", False), ("iid", False),
+                                        ("dense", False), ("systematic", True)])
+def test_bf16_output_is_the_fp32_output_rounded(mode, dedup):
+    """SANTA_OUT_BF16: every element is the fp32 result rounded once to bf16 (ties to
+    even), so it equals the fp32 call's output rounded by torch; empty rows give zeros."""
+    seq = [3000, 0, 1777]
+    _, q, k, v, sl = workloads.small("bf16", 3, 16, 4, 128, 3000, 128, seq_lens=seq, seed=17)
+    qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
+    o32, i32 = santa.decode(qd, kd, vd, sld, 128, mode, seed=4, group_dedup=dedup)
+    o16, i16 = santa.decode(qd, kd, vd, sld, 128, mode, seed=4, group_dedup=dedup, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert o16.dtype == torch.bfloat16
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    assert torch.all(o16[1] == 0)
+    if mode != "dense":
+        assert torch.equal(i16, i32)
+
+
+@pytest.mark.parametrize("mode", ["systematic", "dense"])
+def test_cuda_graph_replay_matches_eager(mode):
+    """santa_decode allocates nothing and never synchronises the host, so a call captured
+    in a CUDA graph (both launches, the programmatic dependency included) replays to the
+    eager result."""
+    _, q, k, v, sl = workloads.small("graph", 2, 32, 8, 128, 8192, 256, seq_lens=[8192, 5000], seed=23)
+    qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
+    shape = santa.make_shape(2, 32, 8, 128, 8192)
+    ws = santa.new_workspace(santa.workspace_size(shape, 256, mode), DEV)
+    ref, iref = santa.decode(qd, kd, vd, sld, 256, mode, seed=9, workspace=ws)
+    out = torch.full_like(ref, float("nan"))
+    idx = torch.full((2, 32, 256), -7, dtype=torch.int32, device=DEV) if mode != "dense" else None
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            santa.decode(qd, kd, vd, sld, 256, mode, seed=9, out=out, idx_out=idx, workspace=ws, stream=s)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+        if idx is not None:
+            assert torch.equal(idx, iref)
+
+
 def test_repeated_calls_are_deterministic_and_leave_counters_clean():
     w, q, k, v, sl = workloads.small("rep", 3, 32, 8, 128, 4096, 256, seq_lens=[4096, 100, 4000], seed=5)
     a = run(q, k, v, sl, 256, "systematic", seed=1)
