@@ -166,6 +166,43 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_le
     return out, (idx_out if m != DENSE else None)
 
 
+class DecodePlan:
+    """santa_decode with every argument but the seed marshalled once: the checks of
+    decode(), the shape, the workspace and the ctypes arguments are built in the
+    constructor, and each call is one foreign call.  For decode loops where the tensors
+    stay put (the call reads whatever the tensors hold at that time)."""
+
+    def __init__(self, q, k_cache, v_cache, seq_lens, S: int, mode="systematic", scale: float = 0.0,
+                 out: torch.Tensor | None = None, idx_out: torch.Tensor | None = None, want_idx: bool = True,
+                 workspace: torch.Tensor | None = None, stream=None, group_dedup: bool = False,
+                 out_dtype: torch.dtype = torch.float32):
+        m = _mode(mode)
+        # one checked call through decode() fixes every buffer (and runs the step once)
+        self.out, self.idx_out = decode(q, k_cache, v_cache, seq_lens, S, m, 0, scale, out, idx_out, want_idx,
+                                        workspace, stream, group_dedup, out_dtype)
+        B, H_q, d = q.shape
+        _, H_kv, n_max, _ = k_cache.shape
+        self._shape = make_shape(B, H_q, H_kv, d, n_max, scale)
+        nbytes = workspace_size(self._shape, S if m != DENSE else 1, m)
+        ws = workspace if workspace is not None else _cached_workspace(nbytes, q.device, stream)
+        self._keep = (q, k_cache, v_cache, seq_lens, ws)  # the buffers stay alive with the plan
+        flags = m | (GROUP_DEDUP if (group_dedup and m != DENSE) else 0) | \
+            (OUT_BF16 if self.out.dtype == torch.bfloat16 else 0)
+        vp = ctypes.c_void_p
+        self._fn = load().santa_decode
+        self._pre = (ctypes.byref(self._shape), vp(q.data_ptr()), vp(k_cache.data_ptr()), vp(v_cache.data_ptr()),
+                     vp(seq_lens.data_ptr()), int(S), flags)
+        self._post = (vp(self.out.data_ptr()),
+                      vp(self.idx_out.data_ptr() if (self.idx_out is not None and m != DENSE) else 0),
+                      vp(ws.data_ptr()), ws.numel(), vp(_stream_ptr(stream)))
+
+    def __call__(self, seed: int):
+        rc = self._fn(*self._pre, ctypes.c_uint64(seed), *self._post)
+        if rc != 0:
+            _check(rc, "santa_decode")
+        return self.out, self.idx_out
+
+
 def sample_points(B: int, H_q: int, S: int, mode, seed: int, device="cuda", stream=None) -> torch.Tensor:
     t = torch.empty(B, H_q, S, dtype=torch.float64, device=device)
     _check(load().santa_sample_points(int(B), int(H_q), int(S), _mode(mode), ctypes.c_uint64(seed),

@@ -186,6 +186,23 @@ def test_cuda_graph_replay_matches_eager(mode):
             assert torch.equal(idx, iref)
 
 
+@pytest.mark.parametrize("mode", ["systematic", "dense"])
+def test_decode_plan_matches_decode(mode):
+    """DecodePlan (arguments marshalled once, one foreign call per step) gives decode()'s
+    results for each seed."""
+    _, q, k, v, sl = workloads.small("plan", 2, 32, 8, 128, 4096, 256, seq_lens=[4096, 999], seed=29)
+    qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
+    plan = santa.DecodePlan(qd, kd, vd, sld, 256, mode)
+    for seed in (3, 4):
+        o1, i1 = plan(seed)
+        o1, i1 = o1.clone(), (i1.clone() if i1 is not None else None)
+        o2, i2 = santa.decode(qd, kd, vd, sld, 256, mode, seed=seed)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2)
+        if mode != "dense":
+            assert torch.equal(i1, i2)
+
+
 def test_repeated_calls_are_deterministic_and_leave_counters_clean():
     w, q, k, v, sl = workloads.small("rep", 3, 32, 8, 128, 4096, 256, seq_lens=[4096, 100, 4000], seed=5)
     a = run(q, k, v, sl, 256, "systematic", seed=1)
