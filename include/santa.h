@@ -124,6 +124,18 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache,
                  size_t workspace_bytes, void *stream);
 
 /*
+ * santa_set_wait_limit -- how long a kernel's pipeline wait (a thread waiting on a
+ * shared-memory barrier for a copy, an MMA or another warp) may last before the kernel
+ * gives up: it sets SANTA_DEV_TIMEOUT in the device error word, winds its roles down
+ * (asynchronous copies and MMAs still in flight are always waited for, up to 2 s) and
+ * exits, leaving the context usable.  Applies to calls made after it, process-wide.
+ * limit_ns = 0 restores the default of 2 s.  A diagnostic: a short limit makes the
+ * timeout path run (the library's tests do that), normal use never needs it.
+ * Returns SANTA_OK.
+ */
+int santa_set_wait_limit(uint64_t limit_ns);
+
+/*
  * santa_sample_points -- the fp64 sample points t [B, H_q, S] (device) that santa_decode
  * uses for (mode, seed), computed by the same device code.  For checking the sampler's
  * random stream against an independent implementation.  mode must be a sampling mode.

@@ -1,6 +1,7 @@
 // santa_api.cu -- the C ABI of libsanta.so (declared in include/santa.h): argument
 // checks, workspace carve-up, split planning and kernel dispatch.  No allocation, no
 // host synchronisation (except santa_device_status), no CPU fallback.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -86,6 +87,7 @@ const void *points_iid_kernel() { return (const void *)santa_points_iid_kernel; 
 
 constexpr int MAX_DEV_STATIC = 64;
 std::mutex g_static_mu;
+std::atomic<unsigned long long> g_wait_limit_ns{0};  // 0: the default of 2 s
 
 namespace {
 
@@ -336,7 +338,8 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     p.k2_hi = (float)k2;
     p.k2_lo = (float)(k2 - (double)p.k2_hi);
     p.tau2 = (float)(3.0 * 1.4426950408889634);  // re-score keys within e^-3 of the maximum
-    p.wait_ns = 2000000000ull;
+    const unsigned long long wlim = g_wait_limit_ns.load(std::memory_order_relaxed);
+    p.wait_ns = wlim ? wlim : 2000000000ull;
 
     const int kind = dense ? KIND_DENSE : KIND_SCORE;
     const void *fn = (D == 128) ? kernel_d128(kind, G) : kernel_d64(kind, G);
@@ -424,6 +427,12 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
         }
         if (cudaLaunchKernelExC(&cfg, fn2, args) != cudaSuccess) return SANTA_ERR_CUDA;
     }
+    return SANTA_OK;
+}
+
+int santa_set_wait_limit(uint64_t limit_ns)
+{
+    g_wait_limit_ns.store((unsigned long long)limit_ns, std::memory_order_relaxed);
     return SANTA_OK;
 }
 

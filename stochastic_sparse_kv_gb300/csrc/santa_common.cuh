@@ -28,6 +28,10 @@ constexpr int SMAX = 4096;           // samples per (b, h)
 enum : int { CTRL_ERR = 0, CTRL_WORK = 1, CTRL_EXIT = 2, CTRL_GROUPS = 64 };
 constexpr int DEV_BAD_SEQLEN = 1;
 constexpr int DEV_TIMEOUT = 2;
+// Limit of the end-of-kernel drains (MMAs still running, TMA fills not yet consumed):
+// never the caller's shorter limit, so that an aborted CTA frees TMEM and exits only
+// after its asynchronous work has completed.
+constexpr uint64_t DRAIN_NS = 2000000000ull;
 
 enum : int { MODE_DENSE = 0, MODE_STRATIFIED = 1, MODE_SYSTEMATIC = 2, MODE_IID = 3 };
 
@@ -86,7 +90,7 @@ struct Params {
     double rS;        // fp64 value nearest 1/S
     float k2_hi, k2_lo;  // scale*log2(e) as an unevaluated fp32 sum
     float tau2;       // re-scoring window below the maximum (log2 units)
-    uint64_t wait_ns; // bounded-wait limit
+    uint64_t wait_ns; // bounded-wait limit of the main loops (santa_set_wait_limit)
 };
 
 // out[i] = v, as fp32 or rounded once to bf16 (round to nearest, ties to even).

@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(DN_NT, 1)
                 mbar_arrive(&tfull[a]);  // (releases adesc[a])
             }
             tc_commit(drain);
-            mbar_wait_bounded(drain, 0u, p.wait_ns);
+            mbar_wait_bounded(drain, 0u, DRAIN_NS);
         }
         __syncwarp();
     } else {
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(DN_NT, 1)
     if (warp == DN_WARP_PROD && lane == 0) {
         const int nfill = (int)tmem_slot[2];
         for (int f = (int)tmem_slot[1]; f < nfill; ++f)
-            if (!mbar_wait_bounded(&full[f % NS], (uint32_t)(f / NS) & 1u, p.wait_ns)) break;
+            if (!mbar_wait_bounded(&full[f % NS], (uint32_t)(f / NS) & 1u, DRAIN_NS)) break;
     }
     if (warp == DN_WARP_MMA) {
         tc_fence_after();

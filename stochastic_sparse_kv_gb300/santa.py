@@ -24,7 +24,8 @@ DEV_BAD_SEQLEN, DEV_TIMEOUT = 1, 2
 
 # every symbol include/santa.h declares
 EXPORTS = ("santa_workspace_size", "santa_workspace_init", "santa_decode", "santa_sample_points",
-           "santa_device_status", "santa_status_string", "santa_version", "santa_decode_static")
+           "santa_device_status", "santa_status_string", "santa_version", "santa_decode_static",
+           "santa_set_wait_limit")
 ERR_SCRATCH = -7
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -71,6 +72,8 @@ def load(path: str | None = None):
         lib.santa_status_string.restype = ctypes.c_char_p
         lib.santa_decode_static.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, vp, i32, i32, u64, vp, vp, vp]
         lib.santa_decode_static.restype = ctypes.c_int
+        lib.santa_set_wait_limit.argtypes = [u64]
+        lib.santa_set_wait_limit.restype = ctypes.c_int
         lib.santa_version.argtypes = []
         lib.santa_version.restype = ctypes.c_int
         _lib = lib
@@ -201,6 +204,12 @@ class DecodePlan:
         if rc != 0:
             _check(rc, "santa_decode")
         return self.out, self.idx_out
+
+
+def set_wait_limit(limit_ns: int) -> None:
+    """santa_set_wait_limit: how long a kernel's pipeline waits may last before it gives
+    up with SANTA_DEV_TIMEOUT (0: the default of 2 s).  A diagnostic knob."""
+    _check(load().santa_set_wait_limit(ctypes.c_uint64(int(limit_ns))), "santa_set_wait_limit")
 
 
 def sample_points(B: int, H_q: int, S: int, mode, seed: int, device="cuda", stream=None) -> torch.Tensor:
