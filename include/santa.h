@@ -13,8 +13,10 @@
  *
  * Conventions for every entry point:
  *  - Device pointers are plain CUDA device addresses; ownership stays with the caller.
- *    The library allocates nothing and keeps no state between calls beyond what it
- *    writes into the caller's workspace.
+ *    The library allocates nothing.  Between calls it keeps only the caller's workspace
+ *    contents, a per-device cache of device attributes and kernel settings, and the
+ *    wait limit of santa_set_wait_limit (santa_decode_static adds its own static
+ *    scratch).
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is enqueued
  *    asynchronously on it; the library never synchronises the host, except in
  *    santa_device_status.
@@ -74,7 +76,8 @@ typedef struct {
     int32_t H_q;    /* query heads */
     int32_t H_kv;   /* KV heads; G = H_q / H_kv must be 1, 2, 4 or 8 */
     int32_t d;      /* head dimension: 64 or 128 */
-    int32_t n_max;  /* KV-cache capacity per (b, h_kv), 1..524288 */
+    int32_t n_max;  /* KV-cache capacity per (b, h_kv), 1..524288; B * H_kv * n_max < 2^31
+                     * (cache rows are addressed with 32-bit tensor-copy coordinates) */
     float scale;    /* score scale */
 } santa_shape;
 

@@ -3,8 +3,9 @@
 // "Stochastic Sparse Attention for Memory-Bound Inference" (abstract): sample S << n_k
 // indices from the post-softmax distribution and aggregate only those value rows,
 // scaled by 1/S.  One CTA per (batch row b, query head h), launched as a programmatic
-// dependent of the score kernel (its point generation can overlap the score kernel's
-// tail).  The score kernel left, per 32-key chunk, the fp32 weights w_j in the chunk's
+// dependent of the score kernel: its CTAs take SMs as the score kernel's CTAs leave them
+// and draw their points before the dependency wait.  The score kernel left, per 32-key
+// chunk, the fp32 weights w_j in the chunk's
 // scale 2^-c_t, the chunk total, c_t and the chunk's maximum score.  After the
 // dependency wait the work is a few wide phases, each at most one round trip to memory,
 // in integer or fp32 arithmetic only:
@@ -19,10 +20,12 @@
 //      heaviest keys' fp32 dot-product rounding would otherwise shift every later CDF
 //      boundary;
 //   E. the exact exclusive prefix O_c of the G_c (block scan), Z = the total;
-//   F. one thread per point: T = t Z, i = min{ j : W_j > T } by chunk -> key;
+//   F. one thread per point: T = t Z, i = min{ j : W_j > T } by chunk -> key, and the
+//      selected V row prefetched into L2; then the head's weights and chunk data, read
+//      for the last time, are discarded from L2 (never written back);
 //   G. the distinct sampled rows (ordered compaction of the sorted list), each loaded
 //      once -- 16-byte pieces spread over all threads, all in flight -- and added times
-//      its count; out = sum / S.
+//      its count; out = sum / S (fp32, or rounded once to bf16).
 #pragma once
 
 #include <cooperative_groups.h>
