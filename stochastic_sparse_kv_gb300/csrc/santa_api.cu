@@ -165,6 +165,8 @@ int check_shape(const santa_shape *sh)
     if (sh->d != 64 && sh->d != 128) return SANTA_ERR_UNSUPPORTED;
     if (sh->B > BMAX || sh->H_q > 1024) return SANTA_ERR_UNSUPPORTED;
     if (sh->n_max > NMAX_LIMIT) return SANTA_ERR_UNSUPPORTED;
+    // the kernels address K and V rows with 32-bit tensor-copy coordinates
+    if ((long long)sh->B * sh->H_kv * sh->n_max >= (1ll << 31)) return SANTA_ERR_UNSUPPORTED;
     return SANTA_OK;
 }
 
@@ -298,9 +300,6 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
             }
         }
     }
-    // the kernels address K and V rows with 32-bit TMA coordinates
-    if ((long long)shape->B * shape->H_kv * shape->n_max >= (1ll << 31)) return SANTA_ERR_UNSUPPORTED;
-
     Params p{};
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.q = static_cast<const uint16_t *>(q);

@@ -188,7 +188,8 @@ class DecodePlan:
         self._shape = make_shape(B, H_q, H_kv, d, n_max, scale)
         nbytes = workspace_size(self._shape, S if m != DENSE else 1, m)
         ws = workspace if workspace is not None else _cached_workspace(nbytes, q.device, stream)
-        self._keep = (q, k_cache, v_cache, seq_lens, ws)  # the buffers stay alive with the plan
+        # the buffers (and the stream object, if one was given) stay alive with the plan
+        self._keep = (q, k_cache, v_cache, seq_lens, ws, stream)
         flags = m | (GROUP_DEDUP if (group_dedup and m != DENSE) else 0) | \
             (OUT_BF16 if self.out.dtype == torch.bfloat16 else 0)
         vp = ctypes.c_void_p

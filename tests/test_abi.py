@@ -65,6 +65,8 @@ def test_workspace_size_matches_layout(lib):
     ((1, 32, 8, 128, 1024), 16, 0x402, -1),     # unknown flag bits
     ((1025, 32, 8, 128, 1024), 16, 2, -4),      # B > 1024
     ((1, 32, 8, 128, 524289), 16, 2, -4),       # n_max too large
+    ((1024, 8, 8, 64, 262144), 16, 2, -4),      # B*H_kv*n_max = 2^31 cache rows: past 32-bit copy coordinates
+    ((1024, 8, 8, 64, 262143), 16, 0, 0),       # one row short of it (dense)
 ])
 def test_workspace_size_validation(lib, shape, S, mode, rc):
     sh = santa.make_shape(*shape)
