@@ -112,3 +112,22 @@ def test_binding_refuses_to_run_without_the_library(tmp_path):
             mod.load(str(tmp_path / "missing.so"))
     finally:
         importlib.reload(santa)
+
+
+def test_wait_limit_setter_is_host_only(lib):
+    # a process-wide setting read by later calls; no device work
+    assert lib.santa_set_wait_limit(ctypes.c_uint64(1000)) == 0
+    assert lib.santa_set_wait_limit(ctypes.c_uint64(0)) == 0
+
+
+def test_binding_checks_tensors_before_calling_the_library():
+    import torch
+    q = torch.zeros(1, 4, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 1, 256, 64, dtype=torch.bfloat16)
+    sl = torch.tensor([256], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        santa.decode(q, k, k, sl, 16, "systematic")          # host tensors
+    with pytest.raises(ValueError, match="CUDA"):
+        santa.DecodePlan(q, k, k, sl, 16, "dense")
+    with pytest.raises(ValueError):
+        santa.decode(q.float(), k, k, sl, 16, "systematic")  # wrong dtype
