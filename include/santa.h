@@ -149,6 +149,8 @@ int santa_sample_points(int32_t B, int32_t H_q, int32_t S, int32_t mode, uint64_
 /*
  * santa_device_status -- synchronise `stream`, read the device error word of the
  * workspace into *code (0 = no error; SANTA_DEV_* bits otherwise) and clear it.
+ * workspace = NULL reads the error word of santa_decode_static's scratch on the current
+ * device instead (*code = 0 when no static call has run on that device).
  * Returns SANTA_OK, or SANTA_ERR_DEVICE when *code != 0.
  */
 int santa_device_status(void *workspace, int32_t *code, void *stream);
@@ -170,13 +172,18 @@ int santa_device_status(void *workspace, int32_t *code, void *stream);
  *
  *  - Size limit: the call returns SANTA_ERR_SCRATCH, before touching the device, when
  *    santa_workspace_size(shape, S, mode) exceeds SANTA_STATIC_SCRATCH_BYTES (for
- *    example B=1, H_q=32, d=128 fits up to about 110k keys).
+ *    example B=1, H_q=32, d=128 fits up to about 110k keys).  Every other argument
+ *    error is also returned before anything is enqueued.
+ *  - Device errors (out-of-range seq_lens, a wait that gave up) set the scratch's own
+ *    error word; santa_device_status(NULL, &code, stream) reads and clears it.  A call
+ *    does not clear it, so it accumulates until read.
  *  - First call per device: it looks up the device address of the scratch array
  *    (cudaGetSymbolAddress, with that device current), which can load the library's
  *    device code.  Make that first call before any stream capture.
- *  - Every call on a device shares the one buffer.  Each call clears the buffer's
- *    control block (an asynchronous memset on `stream`) and overwrites the rest, so
- *    contents left by an earlier call do no harm.  Calls that can overlap on the GPU
+ *  - Every call on a device shares the one buffer.  Each call clears the work counters
+ *    of the buffer's control block (an asynchronous memset on `stream`; the error word is
+ *    left for santa_device_status) and overwrites the rest, so contents left by an
+ *    earlier call, of any shape or mode, do no harm.  Calls that can overlap on the GPU
  *    (different streams without ordering, or several host threads) race on the buffer:
  *    order them on one stream.
  */

@@ -179,6 +179,26 @@ int check_mode_S(int32_t mode_flags, int32_t S)
     return SANTA_OK;
 }
 
+// Every host-side check of a decode call except those on the workspace: shape, mode, S,
+// the tensor pointers and their alignment, and the control block's size.  Nothing is
+// enqueued before these pass (santa_decode and santa_decode_static both call it first).
+int check_decode_args(const santa_shape *shape, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *seq_lens, int32_t S, int32_t mode_flags, const float *out,
+                      const int32_t *idx_out)
+{
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if ((rc = check_mode_S(mode_flags, S))) return rc;
+    if (!q || !k_cache || !v_cache || !seq_lens || !out) return SANTA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(seq_lens, 4) || (idx_out && !aligned(idx_out, 4)))
+        return SANTA_ERR_MISALIGNED;
+    const WsLayout wl = ws_layout(shape->B, shape->H_q, shape->H_kv, shape->d, shape->n_max,
+                                  (mode_flags & 0xff) == SANTA_DENSE);
+    if (wl.ctrl + sizeof(int) * (CTRL_GROUPS + (size_t)shape->B * shape->H_kv) > 65536) return SANTA_ERR_UNSUPPORTED;
+    return SANTA_OK;
+}
+
 // cuTensorMapEncodeTiled from the driver, found once through the runtime (no link
 // against libcuda).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -270,19 +290,14 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
                  const int32_t *seq_lens, int32_t S, int32_t mode_flags, uint64_t seed, float *out, int32_t *idx_out,
                  void *workspace, size_t workspace_bytes, void *stream)
 {
-    int rc = check_shape(shape);
+    int rc = check_decode_args(shape, q, k_cache, v_cache, seq_lens, S, mode_flags, out, idx_out);
     if (rc) return rc;
-    if ((rc = check_mode_S(mode_flags, S))) return rc;
     const int32_t mode = mode_flags & 0xff;
-    if (!q || !k_cache || !v_cache || !seq_lens || !out) return SANTA_ERR_INVALID_ARG;
     if (!workspace) return SANTA_ERR_WORKSPACE;
-    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-        !aligned(seq_lens, 4) || (idx_out && !aligned(idx_out, 4)) || !aligned(workspace, 256))
-        return SANTA_ERR_MISALIGNED;
+    if (!aligned(workspace, 256)) return SANTA_ERR_MISALIGNED;
     const bool dense = (mode == SANTA_DENSE);
     const WsLayout wl = ws_layout(shape->B, shape->H_q, shape->H_kv, shape->d, shape->n_max, dense);
     if (workspace_bytes < wl.total) return SANTA_ERR_WORKSPACE;
-    if (wl.ctrl + sizeof(int) * (CTRL_GROUPS + (size_t)shape->B * shape->H_kv) > 65536) return SANTA_ERR_UNSUPPORTED;
 
     int dev, sms, optin;
     if ((rc = device_info(&dev, &sms, &optin))) return rc;
@@ -456,9 +471,22 @@ int santa_sample_points(int32_t B, int32_t H_q, int32_t S, int32_t mode, uint64_
     return e == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
 }
 
+// The static scratch of santa_decode_static on the current device (defined below), or
+// NULL when no static call has run on it yet.
+static int static_scratch_ptr(void **ptr, bool create);
+
 int santa_device_status(void *workspace, int32_t *code, void *stream)
 {
-    if (!workspace || !code) return SANTA_ERR_INVALID_ARG;
+    if (!code) return SANTA_ERR_INVALID_ARG;
+    if (!workspace) {
+        // the static scratch of santa_decode_static on the current device
+        const int rc = static_scratch_ptr(&workspace, false);
+        if (rc) return rc;
+        if (!workspace) {  // no static call has run on this device: nothing to report
+            *code = 0;
+            return SANTA_OK;
+        }
+    }
     cudaStream_t s = (cudaStream_t)stream;
     int32_t v = 0;
     if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return SANTA_ERR_CUDA;
@@ -478,39 +506,50 @@ int santa_device_status(void *workspace, int32_t *code, void *stream)
 // The scratch buffer of santa_decode_static: a file-scope device array, so that callers
 // that may not allocate device memory can still run a decode step.  Host code must not
 // use its name as an address: the device address comes from cudaGetSymbolAddress, once
-// per device, with that device current.
+// per device, with that device current.  Like every __device__ variable without an
+// initialiser it starts zeroed, so its error word reads 0 before the first call.
 static __device__ __align__(256) unsigned char g_static_scratch[SANTA_STATIC_SCRATCH_BYTES];
 
 namespace {
 void *g_static_ptr[santa::MAX_DEV_STATIC];
 }
 
+// The device address of the scratch on the current device.  With create, the first
+// call on a device looks it up (cudaGetSymbolAddress); without, *ptr is NULL until then.
+static int static_scratch_ptr(void **ptr, bool create)
+{
+    *ptr = nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SANTA_ERR_CUDA;
+    if (dev < 0 || dev >= santa::MAX_DEV_STATIC) return SANTA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(santa::g_static_mu);
+    if (!g_static_ptr[dev] && create) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return SANTA_ERR_CUDA;
+        g_static_ptr[dev] = p;
+    }
+    *ptr = g_static_ptr[dev];
+    return SANTA_OK;
+}
+
 int santa_decode_static(const santa_shape *shape, const void *q, const void *k_cache, const void *v_cache,
                         const int32_t *seq_lens, int32_t S, int32_t mode, uint64_t seed, float *out,
                         int32_t *idx_out, void *stream)
 {
+    // every argument check first: an invalid call enqueues nothing
     size_t need = 0;
     int rc = santa_workspace_size(shape, S, mode, &need);
     if (rc) return rc;
     if (need > SANTA_STATIC_SCRATCH_BYTES) return SANTA_ERR_SCRATCH;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SANTA_ERR_CUDA;
-    if (dev < 0 || dev >= santa::MAX_DEV_STATIC) return SANTA_ERR_UNSUPPORTED;
+    if ((rc = santa::check_decode_args(shape, q, k_cache, v_cache, seq_lens, S, mode, out, idx_out))) return rc;
     void *ws = nullptr;
-    {
-        std::lock_guard<std::mutex> lk(santa::g_static_mu);
-        if (!g_static_ptr[dev]) {
-            void *ptr = nullptr;
-            if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return SANTA_ERR_CUDA;
-            g_static_ptr[dev] = ptr;
-        }
-        ws = g_static_ptr[dev];
-    }
-    // the control block (work counters, error word) must start at zero on every call
-    const santa::WsLayout wl = santa::ws_layout(shape->B, shape->H_q, shape->H_kv, shape->d, shape->n_max,
-                                                (mode & 0xff) == SANTA_DENSE);
+    if ((rc = static_scratch_ptr(&ws, true))) return rc;
+    // The work counters of the control block start at zero on every call (they may hold
+    // anything after a call that gave up early).  Word 0, the device error word, is kept:
+    // santa_device_status(NULL, ...) reads and clears it.
     const size_t ctrl = santa::align_up(sizeof(int) * (santa::CTRL_GROUPS + (size_t)shape->B * shape->H_kv), 256);
-    if (cudaMemsetAsync(ws, 0, ctrl < wl.total ? ctrl : wl.total, (cudaStream_t)stream) != cudaSuccess)
+    if (cudaMemsetAsync(static_cast<uint8_t *>(ws) + sizeof(int), 0, ctrl - sizeof(int), (cudaStream_t)stream) !=
+        cudaSuccess)
         return SANTA_ERR_CUDA;
     return santa_decode(shape, q, k_cache, v_cache, seq_lens, S, mode, seed, out, idx_out, ws,
                         SANTA_STATIC_SCRATCH_BYTES, stream);

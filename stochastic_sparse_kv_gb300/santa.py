@@ -26,6 +26,7 @@ DEV_BAD_SEQLEN, DEV_TIMEOUT = 1, 2
 EXPORTS = ("santa_workspace_size", "santa_workspace_init", "santa_decode", "santa_sample_points",
            "santa_device_status", "santa_status_string", "santa_version", "santa_decode_static",
            "santa_set_wait_limit")
+ERR_DEVICE = -6
 ERR_SCRATCH = -7
 STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -221,8 +222,12 @@ def sample_points(B: int, H_q: int, S: int, mode, seed: int, device="cuda", stre
     return t
 
 
-def device_status(workspace: torch.Tensor, stream=None) -> int:
+def device_status(workspace: torch.Tensor | None, stream=None) -> int:
+    """santa_device_status: the device error word of `workspace` (None: the static scratch
+    of santa_decode_static on the current device), read and cleared."""
     code = ctypes.c_int32(0)
-    load().santa_device_status(ctypes.c_void_p(workspace.data_ptr()), ctypes.byref(code),
-                               ctypes.c_void_p(_stream_ptr(stream)))
+    rc = load().santa_device_status(ctypes.c_void_p(workspace.data_ptr() if workspace is not None else 0),
+                                    ctypes.byref(code), ctypes.c_void_p(_stream_ptr(stream)))
+    if rc not in (OK, ERR_DEVICE):
+        _check(rc, "santa_device_status")
     return int(code.value)

@@ -131,3 +131,25 @@ def test_binding_checks_tensors_before_calling_the_library():
         santa.DecodePlan(q, k, k, sl, 16, "dense")
     with pytest.raises(ValueError):
         santa.decode(q.float(), k, k, sl, 16, "systematic")  # wrong dtype
+
+
+def test_static_entry_point_checks_arguments_before_touching_the_device(lib):
+    """santa_decode_static returns argument errors before it enqueues anything: with no GPU
+    here, any device call would fail with SANTA_ERR_CUDA instead.  The stream is a bogus
+    handle that must never be used."""
+    lib = santa.load()  # (an earlier test reloads the binding module)
+    sh = santa.make_shape(1, 4, 1, 64, 256)
+    good = 4096
+    bogus_stream = ctypes.c_void_p(0xDEAD0)
+
+    def call(q=good, out=good, idx=good, S=16, mode=2):
+        return lib.santa_decode_static(ctypes.byref(sh), ctypes.c_void_p(q), ctypes.c_void_p(good),
+                                       ctypes.c_void_p(good), ctypes.c_void_p(good), S, mode, ctypes.c_uint64(0),
+                                       ctypes.c_void_p(out), ctypes.c_void_p(idx), bogus_stream)
+
+    assert call(q=0) == -1
+    assert call(out=0) == -1
+    assert call(out=good + 4) == -2
+    assert call(idx=good + 2) == -2
+    assert call(S=0) == -1
+    assert call(mode=9) == -1
