@@ -56,7 +56,9 @@ def _load():
         lib.oracle_points.argtypes = [ctypes.c_int, i32, u64, i32, i32, vp]
         lib.oracle_points.restype = ctypes.c_int
         lib.oracle_decode.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, i32,
-                                      ctypes.c_int, u64, vp, vp, i32, vp, vp, vp]
+                                      ctypes.c_int, u64, ctypes.c_int, vp, vp, i32, vp, vp, vp]
+        lib.oracle_ternary_query.argtypes = [i32, vp, u64, i32, i32, vp]
+        lib.oracle_ternary_query.restype = i32
         lib.oracle_decode.restype = ctypes.c_int
         lib.oracle_cdf.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, i32, i32, vp, vp]
         lib.oracle_cdf.restype = ctypes.c_int
@@ -109,11 +111,31 @@ def points(mode, S: int, seed: int, b: int, h: int) -> np.ndarray:
     return t
 
 
+def ternary_query(q, seed: int):
+    """Bernoulli qK^T: the ternary draw of every query head, as a bf16 torch tensor
+    [B,H_q,d] (values -a, 0, +a with a = max |q| of the head), and the count of non-zero
+    features per head (int32 [B,H_q])."""
+    import torch
+    qb = _bits(q)
+    B, H_q, d = qb.shape
+    qt = np.zeros_like(qb)
+    nnz = np.zeros((B, H_q), dtype=np.int32)
+    lib = _load()
+    for b in range(B):
+        for h in range(H_q):
+            row = np.ascontiguousarray(qb[b, h])
+            out = np.zeros(d, dtype=np.uint16)
+            nnz[b, h] = lib.oracle_ternary_query(d, _ptr(row), seed, b, h, _ptr(out))
+            qt[b, h] = out
+    return torch.from_numpy(qt.view(np.int16)).view(torch.bfloat16), nnz
+
+
 def decode(q, k, v, seq_lens, S: int, mode, seed: int = 0, scale: float | None = None,
-           t=None, pairs=None, want_idx: bool = True, want_Z: bool = False):
+           t=None, pairs=None, want_idx: bool = True, want_Z: bool = False, bernoulli: bool = False):
     """Oracle decode step.  q [B,H_q,d], k/v [B,H_kv,n_max,d] (bf16 torch tensors or
-    uint16 bit arrays), seq_lens [B] int.  Returns (out fp64 [B,H_q,d], idx int32
-    [B,H_q,S] or None[, Z fp64 [B,H_q]])."""
+    uint16 bit arrays), seq_lens [B] int.  bernoulli: score with each head's ternary
+    query draw (Bernoulli qK^T, seeded by `seed`).  Returns (out fp64 [B,H_q,d], idx
+    int32 [B,H_q,S] or None[, Z fp64 [B,H_q]])."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     B, H_q, d = qb.shape
     _, H_kv, n_max, d2 = kb.shape
@@ -132,7 +154,7 @@ def decode(q, k, v, seq_lens, S: int, mode, seed: int = 0, scale: float | None =
         pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
         npairs = pr.shape[0]
     rc = _load().oracle_decode(B, H_q, H_kv, d, n_max, ctypes.c_float(scale), _ptr(qb), _ptr(kb),
-                               _ptr(vb), _ptr(sl), S if m != DENSE else 0, m, seed, _ptr(tt),
+                               _ptr(vb), _ptr(sl), S if m != DENSE else 0, m, seed, 1 if bernoulli else 0, _ptr(tt),
                                _ptr(pr), npairs, _ptr(out), _ptr(idx), _ptr(Z))
     if rc != 0:
         raise ValueError("oracle_decode: bad arguments")

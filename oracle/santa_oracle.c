@@ -40,6 +40,20 @@
  *
  * Inputs q, K, V arrive as bf16 bit patterns (uint16) and are widened exactly to fp64.
  * sigma is the fp64 value of the fp32 scale the caller passes.
+ *
+ * Bernoulli qK^T (abstract, last sentences: the score stage is sparsified by
+ * "stochastic ternary queries" that reduce key-feature access; the pages give no
+ * formula).  Reading taken, the plainest unbiased one: before scoring, each query head
+ * q (d features) is replaced by one ternary draw q~ with q~_i in {-a, 0, +a},
+ * a = max_i |q_i|, where q~_i = sign(q_i) * a with probability |q_i| / a and 0
+ * otherwise, independently per feature; so E[q~_i] = q_i and E[q~ . k] = q . k for every
+ * key.  The same q~ scores all keys of the head (it is one query), and a score then needs
+ * only the features where q~_i != 0.  The uniform of feature i is the top 32 bits x_i of
+ * word (i mod 4) of the Philox block (floor(i/4), b, h, 4) (domain 4, apart from the
+ * sampling's domains), and the draw keeps the sign when x_i * 2^-32 < |q_i| / a, i.e.
+ * when x_i * a < |q_i| * 2^32: both products are exact in fp64 (x_i has 32 bits, a and
+ * q_i are bf16 values with 8), so the decision has no rounding.  q~ is a vector of bf16
+ * values (a is one), and the rest of the step runs on it unchanged.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -149,12 +163,11 @@ static double bf16_to_double(uint16_t bits)
 /* Scores s[0..n-1] and unnormalised CDF W[0..n-1] (inclusive prefix of
  * w_j = exp(s_j - m)) of one (b, h); returns m via *m_out. */
 static void cdf_one(int32_t H_q, int32_t H_kv, int32_t d, int32_t n_max, double sigma,
-                    const uint16_t *q, const uint16_t *k, int32_t b, int32_t h, int32_t n,
+                    const uint16_t *qh, const uint16_t *k, int32_t b, int32_t h, int32_t n,
                     double *s, double *W, double *m_out)
 {
     const int32_t G = H_q / H_kv;
     const int32_t g = h / G;
-    const uint16_t *qh = q + ((size_t)b * H_q + h) * d;
     const uint16_t *kg = k + ((size_t)b * H_kv + g) * (size_t)n_max * d;
     double m = -INFINITY;
     for (int32_t j = 0; j < n; ++j) {
@@ -170,6 +183,41 @@ static void cdf_one(int32_t H_q, int32_t H_kv, int32_t d, int32_t n_max, double 
         W[j] = acc;
     }
     *m_out = m;
+}
+
+/* Bernoulli qK^T: the ternary draw q~ of one query head qh [d] (bf16 bits) as bf16 bits
+ * qt [d].  Returns the number of non-zero features. */
+int32_t oracle_ternary_query(int32_t d, const uint16_t *qh, uint64_t seed, int32_t b, int32_t h,
+                             uint16_t *qt)
+{
+    double a = 0.0;
+    uint16_t abits = 0;
+    for (int32_t i = 0; i < d; ++i) {
+        const double x = fabs(bf16_to_double(qh[i]));
+        if (x > a) {
+            a = x;
+            abits = (uint16_t)(qh[i] & 0x7fffu);
+        }
+    }
+    const uint64_t key[2] = {seed, 0};
+    uint64_t r[4] = {0, 0, 0, 0};
+    int32_t nnz = 0;
+    for (int32_t i = 0; i < d; ++i) {
+        if (i % 4 == 0) {
+            const uint64_t ctr[4] = {(uint64_t)(i / 4), (uint64_t)b, (uint64_t)h, 4};
+            oracle_philox4x64_10(ctr, key, r);
+        }
+        const double x = (double)(r[i % 4] >> 32);
+        const double qi = fabs(bf16_to_double(qh[i]));
+        /* keep with probability |q_i| / a: x 2^-32 < |q_i| / a  <=>  x a < |q_i| 2^32 */
+        if (a > 0.0 && x * a < qi * 0x1p32) {
+            qt[i] = (uint16_t)((qh[i] & 0x8000u) | abits);
+            ++nnz;
+        } else {
+            qt[i] = 0;
+        }
+    }
+    return nnz;
 }
 
 /* i = min{ j : W_j > T }, clamped to n-1 (plain binary search over a nondecreasing
@@ -192,7 +240,8 @@ static int check_shape(int32_t B, int32_t H_q, int32_t H_kv, int32_t d, int32_t 
 }
 
 /*
- * Full decode step.  mode: 0 dense, 1 stratified, 2 systematic, 3 iid.
+ * Full decode step.  mode: 0 dense, 1 stratified, 2 systematic, 3 iid; ternary != 0
+ * first replaces every query head by its Bernoulli qK^T draw (seeded by `seed`).
  * q [B,H_q,d], k/v [B,H_kv,n_max,d] as bf16 bits; seq_lens [B] (0 <= n_b <= n_max).
  * t_in: optional caller-chosen points [B,H_q,S] replacing the Philox points.
  * pairs: optional list of n_pairs (b,h) pairs to compute (NULL: all B*H_q pairs).
@@ -201,7 +250,7 @@ static int check_shape(int32_t B, int32_t H_q, int32_t H_kv, int32_t d, int32_t 
  */
 int oracle_decode(int32_t B, int32_t H_q, int32_t H_kv, int32_t d, int32_t n_max, float scale,
                   const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                  const int32_t *seq_lens, int32_t S, int mode, uint64_t seed,
+                  const int32_t *seq_lens, int32_t S, int mode, uint64_t seed, int ternary,
                   const double *t_in, const int32_t *pairs, int32_t n_pairs,
                   double *out, int32_t *idx, double *Z_out)
 {
@@ -222,7 +271,8 @@ int oracle_decode(int32_t B, int32_t H_q, int32_t H_kv, int32_t d, int32_t n_max
         double *W = (double *)malloc(sizeof(double) * (size_t)(n_max > 0 ? n_max : 1));
         double *t = (double *)malloc(sizeof(double) * (size_t)Sa);
         double *acc = (double *)malloc(sizeof(double) * (size_t)d);
-        if (!s || !W || !t || !acc) {
+        uint16_t *qt = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)d);
+        if (!s || !W || !t || !acc || !qt) {
 #pragma omp atomic write
             bad = 1;
         }
@@ -247,7 +297,12 @@ int oracle_decode(int32_t B, int32_t H_q, int32_t H_kv, int32_t d, int32_t n_max
                 continue;
             }
             double m;
-            cdf_one(H_q, H_kv, d, n_max, sigma, q, k, b, h, n, s, W, &m);
+            const uint16_t *qh = q + ((size_t)b * H_q + h) * d;
+            if (ternary) {  /* step 1 of Bernoulli qK^T: the ternary query */
+                oracle_ternary_query(d, qh, seed, b, h, qt);
+                qh = qt;
+            }
+            cdf_one(H_q, H_kv, d, n_max, sigma, qh, k, b, h, n, s, W, &m);
             const double Z = W[n - 1];
             if (Z_out) Z_out[(size_t)b * H_q + h] = Z;
             const uint16_t *vg = v + ((size_t)b * H_kv + g) * (size_t)n_max * d;
@@ -276,7 +331,7 @@ int oracle_decode(int32_t B, int32_t H_q, int32_t H_kv, int32_t d, int32_t n_max
                 for (int32_t i = 0; i < d; ++i) o[i] = acc[i] / (double)S;
             }
         }
-        free(s); free(W); free(t); free(acc);
+        free(s); free(W); free(t); free(acc); free(qt);
     }
     return bad ? -1 : 0;
 }
@@ -293,7 +348,7 @@ int oracle_cdf(int32_t B, int32_t H_q, int32_t H_kv, int32_t d, int32_t n_max, f
     if (n == 0) { *m_out = -INFINITY; return 0; }
     double *s = (double *)malloc(sizeof(double) * (size_t)n);
     if (!s) return -1;
-    cdf_one(H_q, H_kv, d, n_max, (double)scale, q, k, b, h, n, s, W, m_out);
+    cdf_one(H_q, H_kv, d, n_max, (double)scale, q + ((size_t)b * H_q + h) * d, k, b, h, n, s, W, m_out);
     free(s);
     return 0;
 }

@@ -445,3 +445,116 @@ def test_oracle_monte_carlo_unbiased_and_variance(mode):
         assert 0.85 < ratio < 1.15
     else:
         assert ratio < 0.9
+
+
+# ----------------------------------------------------------------------------- Bernoulli qK^T
+#
+# "Stochastic Sparse Attention for Memory-Bound Inference", abstract, last sentences:
+# Bernoulli qK^T sampling sparsifies the score stage with stochastic ternary queries.
+# Reading: q~_i in {-a, 0, +a}, a = max |q_i|, P(q~_i = sign(q_i) a) = |q_i| / a, one
+# independent Bernoulli draw per feature, so E[q~] = q (and E[q~ . k] = q . k).
+
+def _head(vals):
+    return bf16(torch.tensor(vals, dtype=torch.float32)).reshape(1, 1, -1)
+
+
+def test_ternary_query_value_set_and_special_cases():
+    g = torch.Generator().manual_seed(5)
+    q = bf16(3.0 * torch.randn(2, 3, 64, generator=g))
+    q[0, 0, 7] = 0.0
+    for seed in range(20):
+        qt, nnz = oracle.ternary_query(q, seed)
+        qf, qtf = q.float(), qt.float()
+        a = qf.abs().amax(-1, keepdim=True)
+        assert torch.all((qtf == 0) | (qtf.abs() == a)), "values outside {-a, 0, +a}"
+        nz = qtf != 0
+        assert torch.all(torch.sign(qtf[nz]) == torch.sign(qf[nz])), "sign flipped"
+        assert qtf[0, 0, 7] == 0, "a zero feature was drawn"
+        top = qf.abs() == a  # probability 1: always kept
+        assert torch.equal(qtf[top], qf[top])
+        assert np.array_equal(nnz, nz.sum(-1).numpy())
+    # every |q_i| equal: every feature kept, q~ = q exactly; q = 0: q~ = 0
+    q_eq = _head([0.5, -0.5, 0.5, 0.5, -0.5, -0.5, 0.5, -0.5])
+    assert torch.equal(oracle.ternary_query(q_eq, 3)[0], q_eq)
+    q0 = _head([0.0] * 8)
+    qt0, nnz0 = oracle.ternary_query(q0, 3)
+    assert torch.all(qt0.float() == 0) and nnz0.sum() == 0
+
+
+def test_ternary_query_unbiased_keep_rates():
+    """Over many seeds, feature i is kept with frequency |q_i|/a (binomial z-score) and the
+    mean of q~_i is q_i (z-score against the sample standard error)."""
+    g = torch.Generator().manual_seed(11)
+    q = bf16(torch.randn(1, 2, 48, generator=g))
+    N = 6000
+    draws = np.stack([oracle.ternary_query(q, seed)[0].float().numpy() for seed in range(N)])
+    qf = q.float().numpy()
+    a = np.abs(qf).max(-1, keepdims=True)
+    p = np.abs(qf) / a
+    kept = (draws != 0).mean(0)
+    se_p = np.sqrt(np.maximum(p * (1 - p), 1e-12) / N)
+    zp = (kept - p) / se_p
+    assert np.abs(zp[p < 1]).max() < 5.0, np.abs(zp).max()
+    assert np.all(kept[p == 1] == 1.0)
+    mean = draws.mean(0)
+    se = draws.std(0, ddof=1) / np.sqrt(N)
+    z = (mean - qf)[se > 0] / se[se > 0]
+    assert np.abs(z).max() < 5.0 and abs(z.mean()) < 0.2
+
+
+def test_ternary_query_features_independent_by_enumeration():
+    """Six features (two Philox blocks): the 64 keep/drop patterns have probability
+    prod p_i or (1 - p_i); the oracle's pattern histogram over 20000 seeds fits it (chi^2).
+    A uniform shared across features, or words reused between blocks, would not."""
+    import itertools
+    q = _head([1.0, -0.5, 0.75, 0.25, -1.0 * 0.625, 0.375])
+    qf = q.float().numpy()[0, 0]
+    p = np.abs(qf) / np.abs(qf).max()
+    N = 20000
+    counts = {}
+    for seed in range(N):
+        pat = tuple((oracle.ternary_query(q, seed)[0].float().numpy()[0, 0] != 0).astype(int))
+        counts[pat] = counts.get(pat, 0) + 1
+    chi2, dof = 0.0, 0
+    for pat in itertools.product((0, 1), repeat=6):
+        pr = float(np.prod([p[i] if pat[i] else 1 - p[i] for i in range(6)]))
+        if pr == 0:
+            assert counts.get(pat, 0) == 0
+            continue
+        e = N * pr
+        chi2 += (counts.get(pat, 0) - e) ** 2 / e
+        dof += 1
+    dof -= 1
+    # chi^2 with dof degrees of freedom: mean dof, sd sqrt(2 dof); 6 sd is far out
+    assert chi2 < dof + 6 * math.sqrt(2 * dof), (chi2, dof)
+
+
+def test_ternary_draw_differs_across_heads_and_seeds():
+    q = bf16(torch.randn(2, 4, 64, generator=torch.Generator().manual_seed(2)))
+    q[:] = q[0, 0]  # every head the same query: only the counter separates the draws
+    qt, _ = oracle.ternary_query(q, 9)
+    flat = qt.float().reshape(8, 64)
+    assert len({tuple(r.tolist()) for r in flat}) == 8
+    assert not torch.equal(oracle.ternary_query(q, 10)[0], qt)
+
+
+@pytest.mark.parametrize("mode", ["dense", "systematic", "stratified", "iid"])
+def test_bernoulli_decode_scores_with_the_ternary_query(mode):
+    """The Bernoulli step comes first: decoding q with it equals decoding its ternary draw
+    without it, exactly (same seed for both draws)."""
+    q, k, v = rand_case(2, 8, 2, 64, 300, seed=41, qstd=2.0)
+    sl = [300, 170]
+    S = 0 if mode == "dense" else 32
+    o1, i1 = oracle.decode(q, k, v, sl, S, mode, seed=6, bernoulli=True)
+    qt, _ = oracle.ternary_query(q, 6)
+    o2, i2 = oracle.decode(qt, k, v, sl, S, mode, seed=6)
+    assert np.array_equal(o1, o2)
+    if mode != "dense":
+        assert np.array_equal(i1, i2)
+    # a query whose features all have the same magnitude is drawn unchanged
+    q_eq = bf16(0.5 * torch.sign(torch.randn(2, 8, 64, generator=torch.Generator().manual_seed(8))))
+    o3, i3 = oracle.decode(q_eq, k, v, sl, S, mode, seed=6, bernoulli=True)
+    o4, i4 = oracle.decode(q_eq, k, v, sl, S, mode, seed=6)
+    assert np.array_equal(o3, o4)
+    if mode != "dense":
+        assert np.array_equal(i3, i4)
