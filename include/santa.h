@@ -66,6 +66,18 @@ extern "C" {
  * For a caller whose next layer consumes bf16 activations. */
 #define SANTA_OUT_BF16 0x200
 
+/* Flag, or-ed into any mode: Bernoulli qK^T ("Stochastic Sparse Attention for
+ * Memory-Bound Inference", abstract, last sentences: stochastic ternary queries sparsify
+ * the score stage).  Before scoring, every query head q is replaced by one ternary draw
+ * q~ (santa_ternary_query, seeded by `seed`): q~_i = sign(q_i) * a with probability
+ * |q_i| / a and 0 otherwise, a = max_i |q_i|, so E[q~] = q and every score is unbiased.
+ * A score then depends only on the key features where q~_i != 0.  With this library's
+ * row-major cache ([..., n_max, d], 256-byte rows for d = 128) those features are
+ * spread over every row, so the call still reads whole rows: the flag changes the
+ * arithmetic, not the bytes read.  The softmax of unbiased scores is itself not
+ * unbiased, so the output estimates attention under the drawn query. */
+#define SANTA_BERNOULLI_QK 0x400
+
 /* Device error bits (santa_device_status). */
 #define SANTA_DEV_BAD_SEQLEN 1      /* some seq_lens[b] outside [0, n_max]; treated as 0 */
 #define SANTA_DEV_TIMEOUT 2         /* a bounded wait on a shared-memory barrier gave up */
@@ -105,8 +117,9 @@ int santa_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
  *            and set SANTA_DEV_BAD_SEQLEN in the device error word
  *  S         samples per (b, h): 1..4096 (ignored for SANTA_DENSE)
  *  mode      SANTA_DENSE, SANTA_STRATIFIED, SANTA_SYSTEMATIC or SANTA_IID, optionally
- *            or-ed with SANTA_GROUP_DEDUP and SANTA_OUT_BF16
- *  seed      Philox4x64-10 key word 0 (ignored for SANTA_DENSE)
+ *            or-ed with SANTA_GROUP_DEDUP, SANTA_OUT_BF16 and SANTA_BERNOULLI_QK
+ *  seed      Philox4x64-10 key word 0 (ignored for SANTA_DENSE, except for the ternary
+ *            query draws of SANTA_BERNOULLI_QK)
  *  out       device fp32 [B, H_q, d] (bf16 with SANTA_OUT_BF16); n_b = 0 gives zeros
  *  idx_out   device int32 [B, H_q, S] or NULL: the sampled key indices of each (b, h),
  *            ascending, with repeats; n_b = 0 gives -1 (ignored for SANTA_DENSE)
@@ -145,6 +158,19 @@ int santa_set_wait_limit(uint64_t limit_ns);
  */
 int santa_sample_points(int32_t B, int32_t H_q, int32_t S, int32_t mode, uint64_t seed,
                         double *t_out, void *stream);
+
+/*
+ * santa_ternary_query -- the Bernoulli qK^T draws that santa_decode uses with
+ * SANTA_BERNOULLI_QK for this seed, computed by the same device code (for checking the
+ * draw against an independent implementation, and for callers that want q~ itself).
+ *  q       device bf16 [B, H_q, d], contiguous, 16-byte aligned (d = 64 or 128)
+ *  q_out   device bf16 [B, H_q, d]: q~_i in {-a, 0, +a}, a = max_i |q_i| of the head
+ * The uniform of feature i of head (b, h) is the top 32 bits x of word i%4 of the
+ * Philox4x64-10 block with counter (i/4, b, h, 4) and key (seed, 0); the feature keeps
+ * its sign and becomes +-a when x * a < |q_i| * 2^32 (an exact comparison), else 0.
+ */
+int santa_ternary_query(int32_t B, int32_t H_q, int32_t d, const void *q, uint64_t seed, void *q_out,
+                        void *stream);
 
 /*
  * santa_device_status -- synchronise `stream`, read the device error word of the

@@ -80,6 +80,42 @@ __global__ void santa_points_iid_kernel(int B, int H_q, int S, uint64_t seed, do
         t[(size_t)bh * S + s] = __dmul_rn(__uint2double_rn(keys[s]), 0x1p-32);
 }
 
+// Bernoulli qK^T ("Stochastic Sparse Attention for Memory-Bound Inference", abstract,
+// last sentences: stochastic ternary queries sparsify the score stage).  One warp per
+// (b, h): a = max |q_i| over the head, then for each feature i the top 32 bits x of
+// Philox word i%4 of block (i/4, b, h, 4) keep sign(q_i) * a when x * 2^-32 < |q_i| / a,
+// compared as x * a < |q_i| * 2^32 (both products exact in fp64), else 0.  E[q~] = q.
+__global__ void santa_ternary_kernel(int BH, int H_q, int D, uint64_t seed, const uint16_t *q, uint16_t *qt)
+{
+    const int wid = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    if (wid >= BH) return;
+    const int b = wid / H_q, h = wid % H_q;
+    const uint16_t *qh = q + (size_t)wid * D;
+    uint16_t *qo = qt + (size_t)wid * D;
+    // the largest magnitude: for non-negative bf16 values the order of the bit patterns is
+    // that of the values (NaN patterns, above 0x7f80, are left out)
+    uint32_t amax = 0;
+    for (int i = lane; i < D; i += 32) {
+        const uint32_t m = qh[i] & 0x7fffu;
+        if (m <= 0x7f80u) amax = max(amax, m);
+    }
+    amax = __reduce_max_sync(0xffffffffu, amax);
+    const double a = (double)__uint_as_float(amax << 16);
+    for (int i4 = lane; i4 < D / 4; i4 += 32) {
+        uint64_t rnd[4];
+        philox_block(seed, (uint64_t)i4, b, h, 4, rnd);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 4 * i4 + e;
+            const uint32_t bits = qh[i];
+            const double qi = (double)__uint_as_float((bits & 0x7fffu) << 16);
+            const double x = (double)(uint32_t)(rnd[e] >> 32);
+            const bool keep = a > 0.0 && __dmul_rn(x, a) < __dmul_rn(qi, 0x1p32);
+            qo[i] = keep ? (uint16_t)((bits & 0x8000u) | amax) : (uint16_t)0;
+        }
+    }
+}
+
 const void *points_kernel() { return (const void *)santa_points_kernel; }
 const void *points_iid_kernel() { return (const void *)santa_points_iid_kernel; }
 
@@ -172,7 +208,7 @@ int check_shape(const santa_shape *sh)
 
 int check_mode_S(int32_t mode_flags, int32_t S)
 {
-    if (mode_flags & ~(0xff | SANTA_GROUP_DEDUP | SANTA_OUT_BF16)) return SANTA_ERR_INVALID_ARG;
+    if (mode_flags & ~(0xff | SANTA_GROUP_DEDUP | SANTA_OUT_BF16 | SANTA_BERNOULLI_QK)) return SANTA_ERR_INVALID_ARG;
     const int mode = mode_flags & 0xff;
     if (mode < SANTA_DENSE || mode > SANTA_IID) return SANTA_ERR_INVALID_ARG;
     if (mode != SANTA_DENSE && (S < 1 || S > SMAX)) return SANTA_ERR_INVALID_ARG;
@@ -317,6 +353,11 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     }
     Params p{};
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    // Bernoulli qK^T: every step scores with the heads' ternary query draws, which a
+    // first launch writes into the workspace (after every check below has passed)
+    const bool ternary = (mode_flags & SANTA_BERNOULLI_QK) != 0;
+    const void *q_user = q;
+    if (ternary) q = ws + wl.qt;
     p.q = static_cast<const uint16_t *>(q);
     p.k = static_cast<const uint16_t *>(k_cache);
     p.v = static_cast<const uint16_t *>(v_cache);
@@ -379,6 +420,12 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     if (grid < 1) grid = 1;
     void *args[] = {&p};
     const long long krows = (long long)shape->B * shape->H_kv * shape->n_max;
+    if (ternary) {
+        const int BH = shape->B * shape->H_q;
+        santa_ternary_kernel<<<(unsigned)((BH + 7) / 8), 256, 0, (cudaStream_t)stream>>>(
+            BH, shape->H_q, shape->d, seed, static_cast<const uint16_t *>(q_user), reinterpret_cast<uint16_t *>(ws + wl.qt));
+        if (cudaGetLastError() != cudaSuccess) return SANTA_ERR_CUDA;
+    }
     if (dense) {
         // K and V as [B*H_kv*n_max][d] in boxes of a subunit (SC_M rows) and of SC_BOX_ROWS
         // rows (a split's last keys); q in boxes of one group's G heads
@@ -474,6 +521,19 @@ int santa_sample_points(int32_t B, int32_t H_q, int32_t S, int32_t mode, uint64_
 // The static scratch of santa_decode_static on the current device (defined below), or
 // NULL when no static call has run on it yet.
 static int static_scratch_ptr(void **ptr, bool create);
+
+int santa_ternary_query(int32_t B, int32_t H_q, int32_t d, const void *q, uint64_t seed, void *q_out,
+                        void *stream)
+{
+    if (B < 1 || H_q < 1 || !q || !q_out) return SANTA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return SANTA_ERR_UNSUPPORTED;
+    if ((long long)B * H_q > (1ll << 24)) return SANTA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(q_out, 16)) return SANTA_ERR_MISALIGNED;
+    const int BH = B * H_q;
+    santa_ternary_kernel<<<(unsigned)((BH + 7) / 8), 256, 0, (cudaStream_t)stream>>>(
+        BH, H_q, d, seed, static_cast<const uint16_t *>(q), static_cast<uint16_t *>(q_out));
+    return cudaGetLastError() == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
+}
 
 int santa_device_status(void *workspace, int32_t *code, void *stream)
 {

@@ -37,7 +37,7 @@ enum : int { MODE_DENSE = 0, MODE_STRATIFIED = 1, MODE_SYSTEMATIC = 2, MODE_IID 
 
 // Workspace carve-up (byte offsets, each 256-aligned).
 struct WsLayout {
-    size_t ctrl, w, ctot, cexp, cmax, cpre, dpart_o, dpart_ml, total;
+    size_t ctrl, qt, w, ctot, cexp, cmax, cpre, dpart_o, dpart_ml, total;
     int n_pad, nch, ns_max;
 };
 
@@ -53,6 +53,8 @@ __host__ __device__ inline WsLayout ws_layout(int B, int H_q, int H_kv, int d, i
     size_t off = 0;
     L.ctrl = off;
     off = align_up(off + sizeof(int) * (CTRL_GROUPS + (size_t)B * H_kv), 256);
+    L.qt = off;  // Bernoulli qK^T: the ternary query draws, bf16 [B*H_q][d]
+    off = align_up(off + BH * (size_t)d * sizeof(uint16_t), 256);
     if (!dense) {
         L.w = off;    off = align_up(off + BH * L.n_pad * sizeof(float), 256);
         L.ctot = off; off = align_up(off + BH * L.nch * sizeof(float), 256);

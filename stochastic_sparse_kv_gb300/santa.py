@@ -20,12 +20,13 @@ DENSE, STRATIFIED, SYSTEMATIC, IID = 0, 1, 2, 3
 MODES = {"dense": DENSE, "stratified": STRATIFIED, "systematic": SYSTEMATIC, "iid": IID}
 GROUP_DEDUP = 0x100  # or-ed into a sampling mode: V rows loaded once per KV-head group
 OUT_BF16 = 0x200     # or-ed into any mode: out is bf16 (the fp32 result rounded once)
+BERNOULLI_QK = 0x400  # or-ed into any mode: score with each head's ternary query draw
 DEV_BAD_SEQLEN, DEV_TIMEOUT = 1, 2
 
 # every symbol include/santa.h declares
 EXPORTS = ("santa_workspace_size", "santa_workspace_init", "santa_decode", "santa_sample_points",
            "santa_device_status", "santa_status_string", "santa_version", "santa_decode_static",
-           "santa_set_wait_limit")
+           "santa_set_wait_limit", "santa_ternary_query")
 ERR_DEVICE = -6
 ERR_SCRATCH = -7
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -73,6 +74,8 @@ def load(path: str | None = None):
         lib.santa_status_string.restype = ctypes.c_char_p
         lib.santa_decode_static.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, vp, i32, i32, u64, vp, vp, vp]
         lib.santa_decode_static.restype = ctypes.c_int
+        lib.santa_ternary_query.argtypes = [i32, i32, i32, vp, u64, vp, vp]
+        lib.santa_ternary_query.restype = ctypes.c_int
         lib.santa_set_wait_limit.argtypes = [u64]
         lib.santa_set_wait_limit.restype = ctypes.c_int
         lib.santa_version.argtypes = []
@@ -133,12 +136,14 @@ def _cached_workspace(nbytes: int, device, stream) -> torch.Tensor:
 def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens: torch.Tensor,
            S: int, mode="systematic", seed: int = 0, scale: float = 0.0, out: torch.Tensor | None = None,
            idx_out: torch.Tensor | None = None, want_idx: bool = True, workspace: torch.Tensor | None = None,
-           stream=None, group_dedup: bool = False, out_dtype: torch.dtype = torch.float32):
+           stream=None, group_dedup: bool = False, out_dtype: torch.dtype = torch.float32,
+           bernoulli: bool = False):
     """One SANTA (or dense) decode step on the GPU.  q [B,H_q,d], k/v [B,H_kv,n_max,d] bf16,
     seq_lens [B] int32, all on one CUDA device.  Returns (out [B,H_q,d], idx int32
     [B,H_q,S] or None).  out is fp32, or bf16 (SANTA_OUT_BF16) when `out` is a bf16 tensor
     or out_dtype is torch.bfloat16.  group_dedup: load each sampled V row once per group of
-    query heads sharing a KV head (SANTA_GROUP_DEDUP)."""
+    query heads sharing a KV head (SANTA_GROUP_DEDUP).  bernoulli: score with each head's
+    ternary query draw (SANTA_BERNOULLI_QK)."""
     m = _mode(mode)
     B, H_q, d = q.shape
     _, H_kv, n_max, d2 = k_cache.shape
@@ -159,7 +164,8 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_le
         idx_out = torch.empty(B, H_q, S, dtype=torch.int32, device=dev)
     nbytes = workspace_size(shape, S if m != DENSE else 1, m)
     ws = workspace if workspace is not None else _cached_workspace(nbytes, dev, stream)
-    mf = m | (GROUP_DEDUP if (group_dedup and m != DENSE) else 0) | (OUT_BF16 if out.dtype == torch.bfloat16 else 0)
+    mf = m | (GROUP_DEDUP if (group_dedup and m != DENSE) else 0) | (OUT_BF16 if out.dtype == torch.bfloat16 else 0) \
+        | (BERNOULLI_QK if bernoulli else 0)
     rc = load().santa_decode(ctypes.byref(shape), ctypes.c_void_p(q.data_ptr()),
                              ctypes.c_void_p(k_cache.data_ptr()), ctypes.c_void_p(v_cache.data_ptr()),
                              ctypes.c_void_p(seq_lens.data_ptr()), int(S), mf, ctypes.c_uint64(seed),
@@ -179,11 +185,11 @@ class DecodePlan:
     def __init__(self, q, k_cache, v_cache, seq_lens, S: int, mode="systematic", scale: float = 0.0,
                  out: torch.Tensor | None = None, idx_out: torch.Tensor | None = None, want_idx: bool = True,
                  workspace: torch.Tensor | None = None, stream=None, group_dedup: bool = False,
-                 out_dtype: torch.dtype = torch.float32):
+                 out_dtype: torch.dtype = torch.float32, bernoulli: bool = False):
         m = _mode(mode)
         # one checked call through decode() fixes every buffer (and runs the step once)
         self.out, self.idx_out = decode(q, k_cache, v_cache, seq_lens, S, m, 0, scale, out, idx_out, want_idx,
-                                        workspace, stream, group_dedup, out_dtype)
+                                        workspace, stream, group_dedup, out_dtype, bernoulli)
         B, H_q, d = q.shape
         _, H_kv, n_max, _ = k_cache.shape
         self._shape = make_shape(B, H_q, H_kv, d, n_max, scale)
@@ -192,7 +198,7 @@ class DecodePlan:
         # the buffers (and the stream object, if one was given) stay alive with the plan
         self._keep = (q, k_cache, v_cache, seq_lens, ws, stream)
         flags = m | (GROUP_DEDUP if (group_dedup and m != DENSE) else 0) | \
-            (OUT_BF16 if self.out.dtype == torch.bfloat16 else 0)
+            (OUT_BF16 if self.out.dtype == torch.bfloat16 else 0) | (BERNOULLI_QK if bernoulli else 0)
         vp = ctypes.c_void_p
         self._fn = load().santa_decode
         self._pre = (ctypes.byref(self._shape), vp(q.data_ptr()), vp(k_cache.data_ptr()), vp(v_cache.data_ptr()),
@@ -220,6 +226,18 @@ def sample_points(B: int, H_q: int, S: int, mode, seed: int, device="cuda", stre
                                       ctypes.c_void_p(t.data_ptr()), ctypes.c_void_p(_stream_ptr(stream))),
            "santa_sample_points")
     return t
+
+
+def ternary_query(q: torch.Tensor, seed: int, stream=None) -> torch.Tensor:
+    """santa_ternary_query: each head's Bernoulli qK^T draw (bf16 [B,H_q,d])."""
+    if q.dtype != torch.bfloat16 or not q.is_cuda or not q.is_contiguous() or q.dim() != 3:
+        raise ValueError("q must be a contiguous bf16 CUDA tensor [B, H_q, d]")
+    B, H_q, d = q.shape
+    out = torch.empty_like(q)
+    _check(load().santa_ternary_query(int(B), int(H_q), int(d), ctypes.c_void_p(q.data_ptr()), ctypes.c_uint64(seed),
+                                      ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(_stream_ptr(stream))),
+           "santa_ternary_query")
+    return out
 
 
 def device_status(workspace: torch.Tensor | None, stream=None) -> int:

@@ -356,3 +356,62 @@ def test_unbiased_over_4096_seeds(mode):
     assert (np.abs(z) > 4).sum() <= 2
     assert np.abs(z).max() < 5.5
     assert abs(z.mean()) < 0.1 and 0.85 < z.std() < 1.15
+
+
+# ------------------------------------------------------------------ Bernoulli qK^T
+
+@pytest.mark.parametrize("d,H_q", [(128, 32), (64, 8), (128, 4)])
+def test_ternary_query_bit_exact(d, H_q):
+    """santa_ternary_query against the oracle's draw: every bf16 value identical."""
+    for seed in (0, 7, 2**40 + 3):
+        q = workloads.make_q(3, H_q, d, 3.0, torch.Generator().manual_seed(seed % 1000 + d))
+        q[0, 0, :5] = 0.0
+        got = santa.ternary_query(q.to(DEV), seed).cpu()
+        want, _ = oracle.ternary_query(q, seed)
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16)), seed
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[2], CASES[5], CASES[8]])
+@pytest.mark.parametrize("mode", ["systematic", "stratified", "dense"])
+def test_bernoulli_qk_parity(case, mode):
+    """SANTA_BERNOULLI_QK against the oracle run with its Bernoulli step: indices under the
+    boundary rule (boundaries of the drawn query's CDF), the estimator on the GPU's own
+    indices, and the dense output."""
+    d, H_q, H_kv, n_max, seq, S = case
+    w, q, k, v, sl = workloads.small("bern", len(seq), H_q, H_kv, d, n_max, S, seq_lens=seq, seed=d + H_q + n_max)
+    out, idx = santa.decode(q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV), S, mode, seed=7, bernoulli=True)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    o_ref, i_ref = oracle.decode(q, k, v, sl, S if mode != "dense" else 0, mode, seed=7, bernoulli=True)
+    if mode == "dense":
+        check_dense(o, o_ref)
+        return
+    idx = idx.cpu().numpy()
+    qt, _ = oracle.ternary_query(q, 7)
+    check_indices(idx, i_ref, qt, k, sl, S, mode, 7)
+    nz = [b for b in range(len(seq)) if seq[b] > 0]
+    sl1 = torch.tensor([max(x, 1) for x in seq], dtype=torch.int32)
+    g_ref = oracle.gather(v, sl1, np.where(idx < 0, 0, idx))
+    assert np.abs(o[nz] - g_ref[nz]).max() <= 1e-4
+    same = [(b, h) for b in nz for h in range(H_q) if np.array_equal(idx[b, h], i_ref[b, h])]
+    sel = tuple(np.array(same).T)
+    assert np.abs(o[sel] - o_ref[sel]).max() <= 1e-2
+
+
+@pytest.mark.slow
+def test_bernoulli_qk_llama_b1_32k():
+    w = workloads.LLAMA_B1
+    q, k, v, sl = workloads.make_inputs(w)
+    qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
+    qt, nnz = oracle.ternary_query(q, 3)
+    for mode in ("systematic", "dense"):
+        out, idx = santa.decode(qd, kd, vd, sld, w.S, mode, seed=3, bernoulli=True)
+        torch.cuda.synchronize()
+        o_ref, i_ref = oracle.decode(q, k, v, sl, w.S if mode != "dense" else 0, mode, seed=3, bernoulli=True)
+        if mode == "dense":
+            check_dense(out.cpu().numpy(), o_ref)
+        else:
+            nm, npts = check_indices(idx.cpu().numpy(), i_ref, qt, k, sl, w.S, mode, 3)
+            check_estimator(out.cpu().numpy(), idx.cpu().numpy(), v, sl, o_ref)
+            print(f"\n[bernoulli] b1_32k {mode}: {nm} boundary mismatches of {npts}; "
+                  f"ternary density {nnz.mean() / w.d:.3f}")
