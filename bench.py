@@ -37,7 +37,7 @@ KERNEL_SOURCES = [os.path.join(CSRC, f) for f in ("santa_common.cuh", "santa_sam
                                                    "santa_gather.cuh", "santa_dense.cuh", "santa_api.cu")]
 # The sampled path is two launches chained by programmatic dependent launch (the value
 # stage overlaps the score kernel's tail), so one santa_decode call is timed as the unit.
-ROOFLINE_UNIT = "santa_decode: santa_score_kernel<128,4> + santa_gather_kernel<128> (PDL-chained)"
+ROOFLINE_UNIT = "santa_decode: santa_score_kernel<128,4> + santa_gather_kernel<128,4> (PDL-chained)"
 ROOFLINE_UNIT_DENSE = "santa_decode (dense): santa_dense_kernel<128,4> + santa_dense_merge_kernel<128> (PDL-chained)"
 
 
@@ -270,12 +270,13 @@ def run_ours(args):
 
     plans = {}  # one prepared call per configuration: each step is a single foreign call
 
-    def step_mode(mode, S_=S, seed_box=[0], group_dedup=False):
-        key = (mode, S_, group_dedup)
+    def step_mode(mode, S_=S, seed_box=[0], group_dedup=False, bernoulli=False):
+        key = (mode, S_, group_dedup, bernoulli)
         if key not in plans:
             with_idx = mode != "dense" and S_ == S
             plans[key] = santa.DecodePlan(qd, kd, vd, sld, S_, mode, out=out, idx_out=(idx if with_idx else None),
-                                          want_idx=with_idx, group_dedup=group_dedup, stream=stream)
+                                          want_idx=with_idx, group_dedup=group_dedup, stream=stream,
+                                          bernoulli=bernoulli)
         plan = plans[key]
 
         def f():
@@ -285,6 +286,7 @@ def run_ours(args):
 
     peak, peak_kind = measured_peak()
     mode = args.mode
+    launches_per_step = santa.call_info(santa.make_shape(B, H_q, H_kv, d, w.n_max), S, mode)
     with ClockSampler(local) as clk:
         total_ms, per = time_steps(step_mode(mode), args.steps, args.warmup, stream, dist)
     clocks = clk.summary()
@@ -314,6 +316,29 @@ def run_ours(args):
         sweep[str(S2)] = {"us_per_step": round(tm * 1000 / extra_steps, 2),
                           "frac_of_peak": round(ab / (al * 1e-3) / 1e9 / peak, 4)}
 
+    sweep_strat = {}
+    for S2 in (() if args.no_extras else workloads.BATCHED_S_SWEEP):
+        tm, pm = time_steps(step_mode("stratified", S2), extra_steps, 3, stream, dist)
+        ab = algorithmic_bytes(B, H_q, H_kv, d, seq, S2, "stratified")
+        al = sum(pm) / len(pm)
+        sweep_strat[str(S2)] = {"us_per_step": round(tm * 1000 / extra_steps, 2),
+                                "frac_of_peak": round(ab / (al * 1e-3) / 1e9 / peak, 4)}
+
+    # Bernoulli qK^T (the ternary query draws), same inputs
+    variants = {}
+    for name, kw in (() if args.no_extras else (("bernoulli_qk", {"bernoulli": True}),)):
+        row = {}
+        for m in ("systematic", "dense") if name == "bernoulli_qk" else ("systematic",):
+            tm, _ = time_steps(step_mode(m, **kw), extra_steps, 3, stream, dist)
+            row[m] = round(tm * 1000 / extra_steps, 2)
+        variants[name] = row
+    if "bernoulli_qk" in variants:
+        # the fraction of key features the ternary queries select: per head, and the union
+        # over the G heads that share a KV head (what a feature-major cache could skip)
+        qt = santa.ternary_query(qd, 1).view(B, H_kv, H_q // H_kv, d) != 0
+        variants["bernoulli_qk"]["feature_density_per_head"] = round(float(qt.float().mean()), 4)
+        variants["bernoulli_qk"]["feature_density_per_kv_group"] = round(float(qt.any(2).float().mean()), 4)
+
     # the opt-in group deduplication of V loads (SANTA_GROUP_DEDUP) against the default
     gdd = {}
     for S2 in (() if args.no_extras else (256, 2048)):
@@ -322,6 +347,42 @@ def run_ours(args):
             tm, _ = time_steps(step_mode("systematic", S2, group_dedup=flag), extra_steps, 3, stream, dist)
             row["group_dedup" if flag else "per_head"] = round(tm * 1000 / extra_steps, 2)
         gdd[str(S2)] = row
+
+    # every configuration of the workload table, each mode (inputs drawn on the device)
+    wl = {}
+    if not args.no_extras and not args.no_workloads:
+        for w2, S_list in workload_table(workloads):
+            log(f"[bench] workload {w2.name} ...")
+            q2, k2, v2, sl2 = workloads.make_inputs_device(w2, dev)
+            seq2 = sl2.tolist()
+            o2 = torch.empty(w2.B, w2.H_q, w2.d, dtype=torch.float32, device=dev)
+            for S2 in S_list:
+                for m in ("systematic", "stratified", "dense"):
+                    if m == "dense" and S2 != S_list[-1]:
+                        continue
+                    plan = santa.DecodePlan(q2, k2, v2, sl2, S2, m, out=o2, want_idx=False, stream=stream)
+                    sb = [0]
+
+                    def f(plan=plan, sb=sb):
+                        sb[0] += 1
+                        plan(sb[0])
+                    tm, pm = time_steps(f, extra_steps, 3, stream, dist)
+                    ab = algorithmic_bytes(w2.B, w2.H_q, w2.H_kv, w2.d, seq2, S2, m)
+                    al = sum(pm) / len(pm)
+                    key = f"{w2.name}/{m}" + ("" if m == "dense" else f"/S{S2}")
+                    wl[key] = {"us_per_step": round(tm * 1000 / extra_steps, 2),
+                               "frac_of_peak": round(ab / (al * 1e-3) / 1e9 / peak, 4),
+                               "launches": santa.call_info(santa.make_shape(w2.B, w2.H_q, w2.H_kv, w2.d, w2.n_max),
+                                                           S2, m)}
+                    del plan
+            del q2, k2, v2, sl2, o2
+            torch.cuda.empty_cache()
+        for key in list(wl):
+            if "/dense" in key:
+                continue
+            dk = key.rsplit("/", 2)[0] + "/dense"
+            if dk in wl:
+                wl[key]["speedup_vs_dense"] = round(wl[dk]["us_per_step"] / wl[key]["us_per_step"], 3)
 
     # end to end through the C ABI with host buffers: H2D inputs, decode, D2H result
     e2e = None
@@ -375,16 +436,27 @@ def run_ours(args):
                          "avg_launch_us": round(avg_launch_ms * 1000, 2)},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps * 2,  # score + value stage, or dense + merge
+            "gpu_launches": args.steps * launches_per_step,
             "clocks": clocks,
             "modes": modes,
             "S_sweep_systematic": sweep,
+            "S_sweep_stratified": sweep_strat,
+            "variants_us_per_step": variants,
+            "workloads": wl,
             "group_dedup_us_per_step": gdd,
             "multi_layer": ml,
         }
         print(json.dumps(rec), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def workload_table(workloads):
+    """The configurations timed under `workloads` (each with its S values)."""
+    table = [(workloads.LLAMA_B1, (256,))]
+    table += [(lw, (128, 256)) for lw in workloads.LONG]
+    table.append((workloads.RAGGED, (256,)))
+    return table
 
 
 def pick_workload(name):
@@ -463,6 +535,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the other modes and the S sweep")
     ap.add_argument("--workload", default="llama8b_b16_32k")
     ap.add_argument("--layers", type=int, default=32, help="depth of the multi-layer extra (0: skip it)")
+    ap.add_argument("--no-workloads", action="store_true", help="skip timing the other configurations")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

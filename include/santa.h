@@ -140,6 +140,15 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache,
                  size_t workspace_bytes, void *stream);
 
 /*
+ * santa_call_info -- *launches = the kernel launches one santa_decode call with this
+ * shape, S and mode enqueues (for sizing CUDA graphs and counting work): the score stage
+ * and the value stage (or the dense kernel and its merge), plus the ternary query draw of
+ * SANTA_BERNOULLI_QK.  Host only.  Returns SANTA_OK or the argument errors of
+ * santa_decode.
+ */
+int santa_call_info(const santa_shape *shape, int32_t S, int32_t mode, int32_t *launches);
+
+/*
  * santa_set_wait_limit -- how long a kernel's pipeline wait (a thread waiting on a
  * shared-memory barrier for a copy, an MMA or another warp) may last before the kernel
  * gives up: it sets SANTA_DEV_TIMEOUT in the device error word, winds its roles down

@@ -30,6 +30,8 @@ int dense_smem_bytes(int D, int G, int B)
     return dense_smem(D, G, B).total;
 }
 
+
+
 // ---------------------------------------------------------------- points kernels
 
 __global__ void santa_points_kernel(int B, int H_q, int S, int mode, uint64_t seed, double rS, double *t)
@@ -488,6 +490,16 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
         }
         if (cudaLaunchKernelExC(&cfg, fn2, args) != cudaSuccess) return SANTA_ERR_CUDA;
     }
+    return SANTA_OK;
+}
+
+int santa_call_info(const santa_shape *shape, int32_t S, int32_t mode, int32_t *launches)
+{
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if ((rc = check_mode_S(mode, S))) return rc;
+    if (!launches) return SANTA_ERR_INVALID_ARG;
+    *launches = 2 + ((mode & SANTA_BERNOULLI_QK) ? 1 : 0);
     return SANTA_OK;
 }
 

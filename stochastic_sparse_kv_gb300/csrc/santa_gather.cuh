@@ -5,10 +5,10 @@
 // scaled by 1/S.  One CTA per (batch row b, query head h), launched as a programmatic
 // dependent of the score kernel: its CTAs take SMs as the score kernel's CTAs leave them
 // and draw their points before the dependency wait.  The score kernel left, per 32-key
-// chunk, the fp32 weights w_j in the chunk's
-// scale 2^-c_t, the chunk total, c_t and the chunk's maximum score.  After the
-// dependency wait the work is a few wide phases, each at most one round trip to memory,
-// in integer or fp32 arithmetic only:
+// chunk, the fp32 weights w_j in the chunk's scale 2^-c_t, the chunk total, c_t and the
+// chunk's maximum score.  After the dependency wait the work is a few wide phases, each
+// at most one round trip to memory, in integer or fp32 arithmetic only (written for a team
+// of NTH threads synchronised by one barrier; the kernel's team is its whole CTA):
 //   A. chunk data -> shared memory (left in global memory for very long sequences); the
 //      maximum score M and the largest scale C over the sequence;
 //   B. each chunk total as 64-bit fixed point in the global scale 2^-C,
@@ -49,7 +49,9 @@ struct GatherSmem {
     int t, O, tot, ce, cm, hot, hv, hvw, hist, idx, lead, acc, qf, all, own, recv, misc, total;
 };
 
-__host__ __device__ inline GatherSmem gather_smem(int D, int G, int S, int nch_used, int mode, bool xd)
+// Shared memory of one team's value stage (nth threads; xd: the group-deduplicating
+// gather of the two-pass kernel).
+__host__ __device__ inline GatherSmem gather_smem(int D, int G, int S, int nch_used, int mode, bool xd, int nth = NT)
 {
     GatherSmem s{};
     const int Sp = (mode == MODE_IID) ? next_pow2(S) : S;
@@ -66,7 +68,7 @@ __host__ __device__ inline GatherSmem gather_smem(int D, int G, int S, int nch_u
     s.hist = off; off = (int)align_up((size_t)off + HBINS * 4, 16);
     s.idx = off; off = (int)align_up((size_t)off + Sp * 4, 16);
     s.lead = off; off = (int)align_up((size_t)off + (S + 1) * 4, 16);
-    s.acc = off; off += NT * 8 * 4;  // per-thread partial sums of the gather (8 dims each)
+    s.acc = off; off += nth * 8 * 4;  // per-thread partial sums of the gather (8 dims each)
     s.qf = off; off += D * 4;
     s.all = off; off = (int)align_up((size_t)off + (xd ? G * S * 4 : 0), 16);   // the group's G lists
     s.own = off; off = (int)align_up((size_t)off + (xd ? NWARP * G * D * 4 : 0), 16);  // partial sums
@@ -78,30 +80,136 @@ __host__ __device__ inline GatherSmem gather_smem(int D, int G, int S, int nch_u
 
 enum : int { GM_MAX = 0, GM_CMAX = 1, GM_NHOT = 2, GM_NHV = 3, GM_CNT = 4, GM_SCAN = 8 /* NWARP+1 words */ };
 
-// (four CTAs per SM: all B*H_q CTAs of a B=16, H_q=32 step fit in one wave)
-template <int D, int G>
-__global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
+// Barrier of a team of NTH threads: the whole CTA (BAR = 0) or named barrier BAR.
+template <int BAR, int NTH>
+__device__ __forceinline__ void team_sync()
+{
+    if constexpr (BAR == 0)
+        __syncthreads();
+    else
+        asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(NTH) : "memory");
+}
+
+// Exclusive scan of one int per team thread; the team total via *total.
+template <int BAR, int NTH>
+__device__ __forceinline__ int team_excl_scan(int v, int tid, int *scratch /*NTH/32+1 ints*/, int *total)
+{
+    constexpr int NW = NTH / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    team_sync<BAR, NTH>();
+    if (tid == 0) {
+        int acc = 0;
+        for (int w = 0; w < NW; ++w) {
+            const int t = scratch[w];
+            scratch[w] = acc;
+            acc += t;
+        }
+        scratch[NW] = acc;
+    }
+    team_sync<BAR, NTH>();
+    const int res = scratch[warp] + x - v;
+    *total = scratch[NW];
+    team_sync<BAR, NTH>();
+    return res;
+}
+
+// The checked length of batch row b (out-of-range values count as 0; the score stage
+// flags them in the device error word).
+__device__ __forceinline__ int value_len(const Params &p, int b)
+{
+    const int n = p.seq_lens[b];
+    return (n < 0 || n > p.n_max) ? 0 : n;
+}
+
+// A head of an empty row: out = 0, indices -1.
+template <int D, int NTH>
+__device__ __forceinline__ void value_empty(const Params &p, int bh, int tid)
+{
+    for (int i = tid; i < D; i += NTH) store_out(p, (size_t)bh * D + i, 0.f);
+    if (p.idx_out)
+        for (int i = tid; i < p.S; i += NTH) p.idx_out[(size_t)bh * p.S + i] = -1;
+}
+
+// 0. The points (independent of the scores), the query head in fp32 and the team's
+// counters.  Needs no score-stage result.
+template <int D, int G, int NTH, int BAR>
+__device__ __forceinline__ void value_prologue(const Params &p, int bh, uint8_t *smem, const GatherSmem &lay, int tid)
+{
+    const int H_q = p.H_q, S = p.S;
+    const int b = bh / H_q, h = bh % H_q;
+    uint64_t *tfx = reinterpret_cast<uint64_t *>(smem + lay.t);  // points as 64-bit fractions
+    int *idx = reinterpret_cast<int *>(smem + lay.idx);
+    float *qf = reinterpret_cast<float *>(smem + lay.qf);
+    int *misc = reinterpret_cast<int *>(smem + lay.misc);
+    const int Sp = (p.mode == MODE_IID) ? next_pow2(S) : S;
+    if (p.mode == MODE_IID) {
+        unsigned *uk = reinterpret_cast<unsigned *>(idx);
+        for (int s = tid; s < Sp; s += NTH) {
+            unsigned u = 0xffffffffu;
+            if (s < S) {
+                uint64_t rnd[4];
+                philox_block(p.seed, (uint64_t)(s / 4), b, h, 3, rnd);
+                u = (unsigned)(rnd[s % 4] >> 32);
+            }
+            uk[s] = u;
+        }
+        team_sync<BAR, NTH>();
+        for (int kk = 2; kk <= Sp; kk <<= 1)
+            for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+                for (int s = tid; s < Sp; s += NTH) {
+                    const int q2 = s ^ jj;
+                    if (q2 > s) {
+                        const bool asc = (s & kk) == 0;
+                        const unsigned x = uk[s], y = uk[q2];
+                        if ((x > y) == asc) {
+                            uk[s] = y;
+                            uk[q2] = x;
+                        }
+                    }
+                }
+                team_sync<BAR, NTH>();
+            }
+        for (int s = tid; s < S; s += NTH) tfx[s] = (uint64_t)uk[s] << 32;  // u = x 2^-32 exactly
+    } else {
+        // the fp64 point as a 64-bit fraction (t < 1; the scaling by 2^64 is exact)
+        for (int s = tid; s < S; s += NTH)
+            tfx[s] = __double2ull_rz(__dmul_rn(sample_point(p.mode, p.seed, b, h, s, p.rS), 0x1p64));
+    }
+    for (int i = tid; i < D; i += NTH) qf[i] = __uint_as_float((uint32_t)p.q[(size_t)bh * D + i] << 16);
+    if (tid == 0) {
+        misc[GM_MAX] = INT_MIN;  // below the key of every fp32 value
+        misc[GM_CMAX] = INT_MIN;
+        misc[GM_NHOT] = 0;
+        misc[GM_NHV] = 0;
+        misc[GM_CNT] = 0;
+    }
+}
+
+// Phases A-G of head bh (n >= 1 keys), after the team has synchronised past the wait
+// for the score stage's results.  XD: the group-deduplicating gather (two-pass kernel
+// launched as clusters of the group's G heads).
+template <int D, int G, int NTH, int BAR, bool XD>
+__device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8_t *smem, const GatherSmem &lay,
+                                           int tid)
 {
     constexpr int EPL = D / 32;  // V elements per lane
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NW = NTH / 32;
+    const int lane = tid & 31, warp = tid >> 5;
     const unsigned FULL = 0xffffffffu;
-    const int H_q = p.H_q, S = p.S;  // G = H_q / H_kv (template)
-    const int bh = blockIdx.x;
+    const int H_q = p.H_q, S = p.S;
     const int b = bh / H_q, h = bh % H_q, g = h / G;
-    int n = p.seq_lens[b];
-    if (n < 0 || n > p.n_max) n = 0;  // flagged by the score kernel
-    if (n == 0) {
-        for (int i = tid; i < D; i += NT) store_out(p, (size_t)bh * D + i, 0.f);
-        if (p.idx_out)
-            for (int i = tid; i < S; i += NT) p.idx_out[(size_t)bh * S + i] = -1;
-        return;
-    }
+    (void)h;
     const int nchn = (n + CHUNK - 1) / CHUNK;  // chunks of this sequence
-    const GatherSmem lay = gather_smem(D, G, S, p.nch, p.mode, p.xdedup != 0);
     const bool in_smem = p.nch <= NCH_SMEM;
     const size_t bhc = (size_t)bh * p.nch;
-    uint64_t *tfx = reinterpret_cast<uint64_t *>(smem + lay.t);  // points as 64-bit fractions
+    uint64_t *tfx = reinterpret_cast<uint64_t *>(smem + lay.t);
     // the head's chunk arrays: shared-memory copies, or the workspace itself
     uint64_t *O = in_smem ? reinterpret_cast<uint64_t *>(smem + lay.O) : p.cpre + bhc;
     const float *ctot = in_smem ? reinterpret_cast<const float *>(smem + lay.tot) : p.ctot + bhc;
@@ -116,53 +224,6 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
     float *qf = reinterpret_cast<float *>(smem + lay.qf);
     int *misc = reinterpret_cast<int *>(smem + lay.misc);
     uint64_t *scan64 = reinterpret_cast<uint64_t *>(misc + GM_SCAN);
-    const int Sp = (p.mode == MODE_IID) ? next_pow2(S) : S;
-
-    // ---- 0. points (independent of the scores) and the query head in fp32
-    if (p.mode == MODE_IID) {
-        unsigned *uk = reinterpret_cast<unsigned *>(idx);
-        for (int s = tid; s < Sp; s += NT) {
-            unsigned u = 0xffffffffu;
-            if (s < S) {
-                uint64_t rnd[4];
-                philox_block(p.seed, (uint64_t)(s / 4), b, h, 3, rnd);
-                u = (unsigned)(rnd[s % 4] >> 32);
-            }
-            uk[s] = u;
-        }
-        __syncthreads();
-        for (int kk = 2; kk <= Sp; kk <<= 1)
-            for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-                for (int s = tid; s < Sp; s += NT) {
-                    const int q2 = s ^ jj;
-                    if (q2 > s) {
-                        const bool asc = (s & kk) == 0;
-                        const unsigned x = uk[s], y = uk[q2];
-                        if ((x > y) == asc) {
-                            uk[s] = y;
-                            uk[q2] = x;
-                        }
-                    }
-                }
-                __syncthreads();
-            }
-        for (int s = tid; s < S; s += NT) tfx[s] = (uint64_t)uk[s] << 32;  // u = x 2^-32 exactly
-    } else {
-        // the fp64 point as a 64-bit fraction (t < 1; the scaling by 2^64 is exact)
-        for (int s = tid; s < S; s += NT)
-            tfx[s] = __double2ull_rz(__dmul_rn(sample_point(p.mode, p.seed, b, h, s, p.rS), 0x1p64));
-    }
-    for (int i = tid; i < D; i += NT) qf[i] = __uint_as_float((uint32_t)p.q[(size_t)bh * D + i] << 16);
-    if (tid == 0) {
-        misc[GM_MAX] = INT_MIN;  // below the key of every fp32 value
-        misc[GM_CMAX] = INT_MIN;
-        misc[GM_NHOT] = 0;
-        misc[GM_NHV] = 0;
-        misc[GM_CNT] = 0;
-    }
-
-    pdl_wait();  // the score kernel's results are complete and visible from here on
-    __syncthreads();
 
     // ---- A. chunk data; the maximum score M and the largest chunk scale C
     int mk = INT_MIN, cml = INT_MIN;
@@ -171,7 +232,7 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
         int *ce_s = reinterpret_cast<int *>(smem + lay.ce);
         float *cm_s = reinterpret_cast<float *>(smem + lay.cm);
 #pragma unroll 4
-        for (int c = tid; c < nchn; c += NT) {
+        for (int c = tid; c < nchn; c += NTH) {
             const float t = __ldcg(p.ctot + bhc + c);
             const int e = __ldcg(p.cexp + bhc + c);
             const float m = __ldcg(p.cmax + bhc + c);
@@ -182,7 +243,7 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
             cml = max(cml, e);
         }
     } else {
-        for (int c = tid; c < nchn; c += NT) {
+        for (int c = tid; c < nchn; c += NTH) {
             mk = max(mk, fkey(__ldcg(p.cmax + bhc + c)));
             cml = max(cml, __ldcg(p.cexp + bhc + c));
         }
@@ -193,57 +254,57 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
         atomicMax(misc + GM_MAX, mk);
         atomicMax(misc + GM_CMAX, cml);
     }
-    __syncthreads();
+    team_sync<BAR, NTH>();
     const float M = fkey_inv(misc[GM_MAX]);
     const int Cm = misc[GM_CMAX];
     const float thr = M - p.tau2;  // keys with a score >= thr are re-scored
 
     // ---- B. fixed-point chunk totals in the global scale; hot chunks (unordered list)
     int cnt = 0;
-    for (int c = tid; c < nchn; c += NT) {
+    for (int c = tid; c < nchn; c += NTH) {
         O[c] = fixp(ctot[c], FIX_F + cexp[c] - Cm);
         cnt += cmx[c] >= thr ? 1 : 0;
     }
     cnt = __reduce_add_sync(FULL, cnt);
     if (lane == 0 && cnt) atomicAdd(misc + GM_CNT, cnt);
-    __syncthreads();
+    team_sync<BAR, NTH>();
     int nhot = misc[GM_CNT];
     float hthr = thr;
     if (nhot > HCAP) {
         // too many qualify: keep the hottest, by a histogram of the maxima over
         // [thr, M] read from the top until HCAP would be exceeded
-        for (int i = tid; i < HBINS; i += NT) hist[i] = 0;
-        __syncthreads();
+        for (int i = tid; i < HBINS; i += NTH) hist[i] = 0;
+        team_sync<BAR, NTH>();
         const float span = fmaxf(M - thr, 1e-30f);
-        for (int c = tid; c < nchn; c += NT) {
+        for (int c = tid; c < nchn; c += NTH) {
             const float m = cmx[c];
             if (m >= thr) atomicAdd(hist + min(HBINS - 1, (int)((m - thr) / span * HBINS)), 1);
         }
-        __syncthreads();
+        team_sync<BAR, NTH>();
         if (tid == 0) {
             int acc = 0, bin = HBINS;
             while (bin > 0 && acc + hist[bin - 1] <= HCAP) acc += hist[--bin];
             misc[GM_CNT] = bin;  // lowest bin kept (HBINS: none fits)
         }
-        __syncthreads();
+        team_sync<BAR, NTH>();
         const int bin = misc[GM_CNT];
         hthr = bin < HBINS ? thr + span * ((float)bin / HBINS) : __int_as_float(0x7f800000);
         // (a chunk exactly on a bin edge may land in the bin below: count again)
         int cc = 0;
-        for (int c = tid; c < nchn; c += NT) cc += cmx[c] >= hthr ? 1 : 0;
+        for (int c = tid; c < nchn; c += NTH) cc += cmx[c] >= hthr ? 1 : 0;
         cc = __reduce_add_sync(FULL, cc);
-        __syncthreads();
+        team_sync<BAR, NTH>();
         if (tid == 0) misc[GM_CNT] = 0;
-        __syncthreads();
+        team_sync<BAR, NTH>();
         if (lane == 0 && cc) atomicAdd(misc + GM_CNT, cc);
-        __syncthreads();
+        team_sync<BAR, NTH>();
         nhot = misc[GM_CNT];
         if (nhot > HCAP) nhot = 0;  // (ties at the very top: no re-scoring)
     }
     if (nhot > 0) {
-        for (int c = tid; c < nchn; c += NT)
+        for (int c = tid; c < nchn; c += NTH)
             if (cmx[c] >= hthr) hot[atomicAdd(misc + GM_NHOT, 1)] = c;
-        __syncthreads();
+        team_sync<BAR, NTH>();
     }
 
     // ---- C. heavy keys of the hot chunks: slot q = hot entry * 8 + quarter (four keys,
@@ -252,12 +313,12 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
     float *wrow = p.w + (size_t)bh * p.n_pad;
     const uint16_t *kg = p.k + ((size_t)b * p.H_kv + g) * (size_t)p.n_max * D;
     constexpr int QPC = CHUNK / 4;  // quarters per chunk
-    for (int q0 = tid; q0 < nhot * QPC; q0 += 8 * NT) {
+    for (int q0 = tid; q0 < nhot * QPC; q0 += 8 * NTH) {
         float4 wv[8];
         int jj[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int q = q0 + u * NT;
+            const int q = q0 + u * NTH;
             jj[u] = -1;
             wv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (q < nhot * QPC) {
@@ -286,11 +347,11 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
             }
         }
     }
-    __syncthreads();
+    team_sync<BAR, NTH>();
     const int nhv = min(misc[GM_NHV], HKCAP);
 
     // ---- D. re-score the heavy keys (four lanes each) and patch their chunk totals
-    for (int i0 = 0; i0 < nhv; i0 += NT / 4) {  // (every lane runs every pass: they shuffle)
+    for (int i0 = 0; i0 < nhv; i0 += NTH / 4) {  // (every lane runs every pass: they shuffle)
         const int i = i0 + tid / 4, part = tid & 3;
         const int j = i < nhv ? hv[i] : 0;
         float shi, slo;
@@ -305,11 +366,11 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
             if (dx) atomicAdd((unsigned long long *)(O + c), (unsigned long long)dx);
         }
     }
-    __syncthreads();
+    team_sync<BAR, NTH>();
 
     // ---- E. exact exclusive prefix of the G_c: a contiguous range per thread
     {
-        const int per = (nchn + NT - 1) / NT;
+        const int per = (nchn + NTH - 1) / NTH;
         const int c0 = min(tid * per, nchn), c1 = min(c0 + per, nchn);
         uint64_t run = 0;
         for (int c = c0; c < c1; ++c) run += O[c];
@@ -321,17 +382,17 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
             if (lane >= o) x += y;
         }
         if (lane == 31) scan64[warp] = x;
-        __syncthreads();
+        team_sync<BAR, NTH>();
         if (tid == 0) {
             uint64_t a = 0;
-            for (int w = 0; w < NWARP; ++w) {
+            for (int w = 0; w < NW; ++w) {
                 const uint64_t t = scan64[w];
                 scan64[w] = a;
                 a += t;
             }
-            scan64[NWARP] = a;
+            scan64[NW] = a;
         }
-        __syncthreads();
+        team_sync<BAR, NTH>();
         uint64_t base = scan64[warp] + x - run;
         for (int c = c0; c < c1; ++c) {
             const uint64_t v = O[c];
@@ -339,11 +400,11 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
             base += v;
         }
     }
-    __syncthreads();
-    const uint64_t Z = scan64[NWARP];
+    team_sync<BAR, NTH>();
+    const uint64_t Z = scan64[NW];
 
     // ---- F. points -> chunk (binary search on O) -> key (the chunk's 32 weights, one line)
-    for (int s = tid; s < S; s += NT) {
+    for (int s = tid; s < S; s += NTH) {
         const uint64_t T = __umul64hi(tfx[s], Z);
         int lo = 0, hi = nchn - 1;  // largest c with O_c <= T
         while (lo < hi) {
@@ -381,22 +442,22 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
         prefetch_l2(vrow);
         if (D * 2 > 128) prefetch_l2(vrow + 64);
     }
-    __syncthreads();
+    team_sync<BAR, NTH>();
     // The head's weights and chunk data have been read for the last time: drop them from
     // L2 so that they are never written back (the next step's score stage rewrites them).
-    l2_discard_range(wrow, (size_t)nchn * CHUNK * sizeof(float), tid, NT);
-    l2_discard_range(p.ctot + bhc, (size_t)p.nch * sizeof(float), tid, NT);
-    l2_discard_range(p.cexp + bhc, (size_t)p.nch * sizeof(int), tid, NT);
-    l2_discard_range(p.cmax + bhc, (size_t)p.nch * sizeof(float), tid, NT);
-    if (!in_smem) l2_discard_range(p.cpre + bhc, (size_t)p.nch * sizeof(uint64_t), tid, NT);
+    l2_discard_range(wrow, (size_t)nchn * CHUNK * sizeof(float), tid, NTH);
+    l2_discard_range(p.ctot + bhc, (size_t)p.nch * sizeof(float), tid, NTH);
+    l2_discard_range(p.cexp + bhc, (size_t)p.nch * sizeof(int), tid, NTH);
+    l2_discard_range(p.cmax + bhc, (size_t)p.nch * sizeof(float), tid, NTH);
+    if (!in_smem) l2_discard_range(p.cpre + bhc, (size_t)p.nch * sizeof(uint64_t), tid, NTH);
 
     // ---- G. sorted indices out; each warp gathers the distinct rows of its run of
     // points (a row split between two warps is loaded by both, each with its own count)
     if (p.idx_out)
-        for (int s = tid; s < S; s += NT) p.idx_out[(size_t)bh * S + s] = idx[s];
+        for (int s = tid; s < S; s += NTH) p.idx_out[(size_t)bh * S + s] = idx[s];
     const uint16_t *vg = p.v + ((size_t)b * p.H_kv + g) * (size_t)p.n_max * D;
-    if constexpr (G > 1) {
-        if (p.xdedup) {
+    if constexpr (G > 1 && XD) {
+        {
             // The group's G heads run as one cluster (rank k = head g*G + k).  Each CTA
             // copies the G sorted lists, loads the distinct rows of its own list that no
             // lower-ranked head sampled -- so every row of the group is loaded once -- and
@@ -406,18 +467,18 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
             cg::cluster_group cl = cg::this_cluster();
             const int me = (int)cl.block_rank();
             int *all = reinterpret_cast<int *>(smem + lay.all);      // [G][S]: every head's list
-            float *red = reinterpret_cast<float *>(smem + lay.own);  // [NWARP][G][D] partial sums
+            float *red = reinterpret_cast<float *>(smem + lay.own);  // [NW][G][D] partial sums
             float *recv = reinterpret_cast<float *>(smem + lay.recv);  // [G][D]
             // push this head's sorted list into slot `me` of every CTA of the group
 #pragma unroll
             for (int k = 0; k < G; ++k) {
                 int *dst = cl.map_shared_rank(all, k) + me * S;
-                for (int s = tid; s < S; s += NT) dst[s] = idx[s];
+                for (int s = tid; s < S; s += NTH) dst[s] = idx[s];
             }
             cl.sync();  // every list is everywhere
             // each warp takes a run of points of its own list; a point leads if it is the
             // row's first occurrence here and no lower-ranked head sampled the row
-            const int per = (S + NWARP - 1) / NWARP;
+            const int per = (S + NW - 1) / NW;
             const int s0 = min(warp * per, S), s1 = min(s0 + per, S);
             float acc[G][EPL];
 #pragma unroll
@@ -482,16 +543,16 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
             for (int k = 0; k < G; ++k)
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) red[(warp * G + k) * D + EPL * lane + e] = acc[k][e];
-            __syncthreads();
-            for (int i = tid; i < G * D; i += NT) {
+            team_sync<BAR, NTH>();
+            for (int i = tid; i < G * D; i += NTH) {
                 const int k = i / D, dd = i % D;
                 float sum = 0.f;
 #pragma unroll
-                for (int w = 0; w < NWARP; ++w) sum = __fadd_rn(sum, red[(w * G + k) * D + dd]);
+                for (int w = 0; w < NW; ++w) sum = __fadd_rn(sum, red[(w * G + k) * D + dd]);
                 cl.map_shared_rank(recv, k)[me * D + dd] = sum;
             }
             cl.sync();  // every partial sum has arrived
-            for (int i = tid; i < D; i += NT) {
+            for (int i = tid; i < D; i += NTH) {
                 float sum = 0.f;
 #pragma unroll
                 for (int jj = 0; jj < G; ++jj) sum = __fadd_rn(sum, recv[jj * D + i]);
@@ -503,21 +564,21 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
     // distinct rows of this head's sorted list (first occurrences, in order) ...
     int *lead = reinterpret_cast<int *>(smem + lay.lead);
     {
-        const int per = (S + NT - 1) / NT;
+        const int per = (S + NTH - 1) / NTH;
         const int s0 = min(tid * per, S), s1 = min(s0 + per, S);
         int cnt = 0;
         for (int s = s0; s < s1; ++s) cnt += (s == 0 || idx[s] != idx[s - 1]) ? 1 : 0;
         int nlead;
-        int pos = block_excl_scan(cnt, misc, &nlead);
+        int pos = team_excl_scan<BAR, NTH>(cnt, tid, misc, &nlead);
         for (int s = s0; s < s1; ++s)
             if (s == 0 || idx[s] != idx[s - 1]) lead[pos++] = s;
         if (tid == 0) lead[nlead] = S;
-        __syncthreads();
+        team_sync<BAR, NTH>();
         // ... then each thread loads 16-byte pieces (8 dimensions) of every RSTEP-th
         // distinct row, eight loads in flight, and adds them times their counts; the
         // RSTEP partial sums of each piece are added in a fixed order
         constexpr int NPC = D * 2 / 16;   // 16-byte pieces per row
-        constexpr int RSTEP = NT / NPC;   // rows in parallel
+        constexpr int RSTEP = NTH / NPC;   // rows in parallel
         const int piece = tid % NPC, r0 = tid / NPC;
         float acc[8];
 #pragma unroll
@@ -548,13 +609,36 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc_s[(r0 * NPC + piece) * 8 + e] = acc[e];
-        __syncthreads();
-        for (int i = tid; i < D; i += NT) {
+        team_sync<BAR, NTH>();
+        for (int i = tid; i < D; i += NTH) {
             float sum = 0.f;
             for (int r = 0; r < RSTEP; ++r) sum = __fadd_rn(sum, acc_s[(r * NPC + i / 8) * 8 + i % 8]);
             store_out(p, (size_t)bh * D + i, __fdiv_rn(sum, (float)S));
         }
     }
+}
+
+// One CTA per (b, h_q), a programmatic dependent of the score kernel (four CTAs per SM:
+// all B*H_q CTAs of a B=16, H_q=32 step fit in one wave).  With SANTA_GROUP_DEDUP the host
+// launches the G heads of a group as one cluster.
+template <int D, int G>
+__global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, bh = blockIdx.x;
+    const int n = value_len(p, bh / p.H_q);
+    if (n == 0) {  // (every CTA of a cluster shares b, so all of them leave here)
+        value_empty<D, NT>(p, bh, tid);
+        return;
+    }
+    const GatherSmem lay = gather_smem(D, G, p.S, p.nch, p.mode, p.xdedup != 0);
+    value_prologue<D, G, NT, 0>(p, bh, smem, lay, tid);
+    pdl_wait();  // the score kernel's results are complete and visible from here on
+    __syncthreads();
+    if (p.xdedup)
+        value_main<D, G, NT, 0, true>(p, bh, n, smem, lay, tid);
+    else
+        value_main<D, G, NT, 0, false>(p, bh, n, smem, lay, tid);
 }
 
 }  // namespace santa

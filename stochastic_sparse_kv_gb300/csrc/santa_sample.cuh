@@ -94,35 +94,7 @@ __device__ __forceinline__ void rescore_key_quad(const uint16_t *krow, const flo
     fast_two_sum(P, E, hi, lo);
 }
 
-// ------------------------------------------------------------------ block helpers
-
-// Exclusive block scan of one int per thread; returns the block total via *total.
-__device__ __forceinline__ int block_excl_scan(int v, int *scratch /*NWARP+1 ints*/, int *total)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) scratch[warp] = x;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int acc = 0;
-        for (int w = 0; w < NWARP; ++w) {
-            const int t = scratch[w];
-            scratch[w] = acc;
-            acc += t;
-        }
-        scratch[NWARP] = acc;
-    }
-    __syncthreads();
-    const int res = scratch[warp] + x - v;
-    *total = scratch[NWARP];
-    __syncthreads();
-    return res;
-}
+// ------------------------------------------------------------------ search helpers
 
 __device__ __forceinline__ int lower_bound_i(const int *a, int n, int key)
 {

@@ -26,7 +26,7 @@ DEV_BAD_SEQLEN, DEV_TIMEOUT = 1, 2
 # every symbol include/santa.h declares
 EXPORTS = ("santa_workspace_size", "santa_workspace_init", "santa_decode", "santa_sample_points",
            "santa_device_status", "santa_status_string", "santa_version", "santa_decode_static",
-           "santa_set_wait_limit", "santa_ternary_query")
+           "santa_set_wait_limit", "santa_ternary_query", "santa_call_info")
 ERR_DEVICE = -6
 ERR_SCRATCH = -7
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -76,6 +76,8 @@ def load(path: str | None = None):
         lib.santa_decode_static.restype = ctypes.c_int
         lib.santa_ternary_query.argtypes = [i32, i32, i32, vp, u64, vp, vp]
         lib.santa_ternary_query.restype = ctypes.c_int
+        lib.santa_call_info.argtypes = [ctypes.POINTER(Shape), i32, i32, ctypes.POINTER(i32)]
+        lib.santa_call_info.restype = ctypes.c_int
         lib.santa_set_wait_limit.argtypes = [u64]
         lib.santa_set_wait_limit.restype = ctypes.c_int
         lib.santa_version.argtypes = []
@@ -212,6 +214,15 @@ class DecodePlan:
         if rc != 0:
             _check(rc, "santa_decode")
         return self.out, self.idx_out
+
+
+def call_info(shape: Shape, S: int, mode, group_dedup: bool = False, bernoulli: bool = False) -> int:
+    """santa_call_info: the kernel launches one decode call with this shape, S and mode
+    enqueues."""
+    m = _mode(mode) | (GROUP_DEDUP if group_dedup else 0) | (BERNOULLI_QK if bernoulli else 0)
+    n = ctypes.c_int32(0)
+    _check(load().santa_call_info(ctypes.byref(shape), int(S), m, ctypes.byref(n)), "santa_call_info")
+    return int(n.value)
 
 
 def set_wait_limit(limit_ns: int) -> None:

@@ -115,6 +115,38 @@ def _boost(kb: torch.Tensor, qb: torch.Tensor, w: Workload, gen: torch.Generator
     return kb
 
 
+def make_inputs_device(w: Workload, device, seed: int | None = None):
+    """The same recipe as make_inputs, drawn on `device` with a device generator: the
+    same shapes and distributions (and the same seq_lens), but other random values.  For
+    timing runs over large caches, where drawing on the host would take minutes."""
+    seed = w.seed if seed is None else seed
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    g = torch.randn(w.B, w.H_q, w.d, generator=gen, device=device, dtype=torch.float32)
+    if w.score_std is not None:
+        g = (w.score_std * math.sqrt(w.d) * g.double() / g.double().norm(dim=-1, keepdim=True)).float()
+    q = g.to(torch.bfloat16)
+    shape = (w.B, w.H_kv, w.n_max, w.d)
+    k = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    v = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    for b in range(w.B):
+        kb = torch.randn(shape[1:], generator=gen, device=device, dtype=torch.float32)
+        if w.heavy_frac > 0:
+            qb = q[b].float()
+            G, d = w.G, w.d
+            std = w.score_std if w.score_std is not None else 1.0
+            n_heavy = max(1, int(round(w.heavy_frac * w.n_max)))
+            for hk in range(w.H_kv):
+                qbar = qb[hk * G:(hk + 1) * G].double().mean(0)
+                c = w.heavy_sigmas * std * math.sqrt(d) / float(qbar.norm())
+                pick = torch.randperm(w.n_max, generator=gen, device=device)[:n_heavy]
+                kb[hk, pick] += (c * qbar / qbar.norm()).float()
+        k[b].copy_(kb.to(torch.bfloat16))
+        v[b].copy_(torch.randn(shape[1:], generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16))
+        del kb
+    return q, k, v, seq_lens_for(w).to(device)
+
+
 def small(name: str, B: int, H_q: int, H_kv: int, d: int, n_max: int, S: int, *,
           seq_lens=None, score_std: float | None = 3.0, heavy_frac: float = 0.0, seed: int = 0):
     """An ad-hoc small workload (parity tests): optional explicit seq_lens list."""

@@ -105,6 +105,12 @@ def test_decode_rejects_bad_arguments_on_the_host(lib):
     assert lib.santa_sample_points(1, 1, 1, 0, ctypes.c_uint64(0), ctypes.c_void_p(good), None) == -1
     assert lib.santa_ternary_query(0, 1, 128, ctypes.c_void_p(good), ctypes.c_uint64(0), ctypes.c_void_p(good),
                                    None) == -1
+    n = ctypes.c_int32(0)
+    assert lib.santa_call_info(ctypes.byref(bad), 16, 2, ctypes.byref(n)) == -1
+    assert lib.santa_call_info(ctypes.byref(sh), 0, 2, ctypes.byref(n)) == -1
+    assert lib.santa_call_info(ctypes.byref(sh), 16, 2, None) == -1
+    assert lib.santa_call_info(ctypes.byref(sh), 16, 2, ctypes.byref(n)) == 0 and n.value == 2
+    assert lib.santa_call_info(ctypes.byref(sh), 16, 0x402, ctypes.byref(n)) == 0 and n.value == 3
     assert lib.santa_ternary_query(1, 1, 96, ctypes.c_void_p(good), ctypes.c_uint64(0), ctypes.c_void_p(good),
                                    None) == -4
     assert lib.santa_ternary_query(1, 1, 128, ctypes.c_void_p(good + 2), ctypes.c_uint64(0),

@@ -415,3 +415,13 @@ def test_bernoulli_qk_llama_b1_32k():
             check_estimator(out.cpu().numpy(), idx.cpu().numpy(), v, sl, o_ref)
             print(f"\n[bernoulli] b1_32k {mode}: {nm} boundary mismatches of {npts}; "
                   f"ternary density {nnz.mean() / w.d:.3f}")
+
+
+# ------------------------------------------------------------------ launch count
+
+def test_call_info_counts_the_launches_of_a_call():
+    sh = santa.make_shape(16, 32, 8, 128, 32768)
+    assert santa.call_info(sh, 256, "systematic") == 2
+    assert santa.call_info(sh, 256, "stratified", bernoulli=True) == 3
+    assert santa.call_info(sh, 256, "systematic", group_dedup=True) == 2
+    assert santa.call_info(sh, 1, "dense") == 2
