@@ -150,8 +150,10 @@ def dist_setup(n_gpus):
 
 
 def time_steps(fn, steps, warmup, stream, dist=None):
-    """W untimed steps, then exactly `steps` timed steps bracketed by barrier + sync;
-    returns (total ms over the max of ranks, per-launch event ms list)."""
+    """W untimed steps, then exactly `steps` timed steps bracketed by barrier + sync and one
+    pair of CUDA events on the launching stream (no events between the steps: at small
+    batches their own cost would show); returns (total ms over the max of ranks, the mean
+    ms of one step on this rank, repeated per step)."""
     import torch
     for _ in range(warmup):
         fn()
@@ -159,19 +161,17 @@ def time_steps(fn, steps, warmup, stream, dist=None):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for a, b in evs:
-        a.record(stream)
+    for _ in range(steps):
         fn()
-        b.record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
-    total = max_over_ranks(t0.elapsed_time(t1), dist, "cuda")
+    local = t0.elapsed_time(t1)
+    total = max_over_ranks(local, dist, "cuda")
     torch.cuda.synchronize()
-    return total, [a.elapsed_time(b) for a, b in evs]
+    return total, [local / steps] * steps
 
 
 def max_over_ranks(value, dist=None, device="cpu"):

@@ -78,6 +78,17 @@ extern "C" {
  * unbiased, so the output estimates attention under the drawn query. */
 #define SANTA_BERNOULLI_QK 0x400
 
+/* Flag, or-ed into a sampling mode: always use the two launches of the score and value
+ * stages.  By default a small problem runs as one launch of the single-pass kernel
+ * instead: one thread-block cluster of up to 16 CTAs per (batch row, KV head), with the
+ * softmax weights and CDF kept in shared memory and the value stage done inside the
+ * cluster.  It applies when the B * H_kv clusters fit the GPU at once with at most 4096
+ * keys per CTA and G * S <= 2048 (for example B = 1 up to about 48k keys, or B = 4 up to
+ * 8k keys, at H_kv = 8 on a GB300); santa_call_info reports which one runs.  Indices
+ * are the same either way; outputs differ only by the order of the fp32 additions of
+ * the gather. */
+#define SANTA_TWO_PASS 0x800
+
 /* Device error bits (santa_device_status). */
 #define SANTA_DEV_BAD_SEQLEN 1      /* some seq_lens[b] outside [0, n_max]; treated as 0 */
 #define SANTA_DEV_TIMEOUT 2         /* a bounded wait on a shared-memory barrier gave up */
@@ -117,7 +128,8 @@ int santa_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
  *            and set SANTA_DEV_BAD_SEQLEN in the device error word
  *  S         samples per (b, h): 1..4096 (ignored for SANTA_DENSE)
  *  mode      SANTA_DENSE, SANTA_STRATIFIED, SANTA_SYSTEMATIC or SANTA_IID, optionally
- *            or-ed with SANTA_GROUP_DEDUP, SANTA_OUT_BF16 and SANTA_BERNOULLI_QK
+ *            or-ed with SANTA_GROUP_DEDUP, SANTA_OUT_BF16, SANTA_BERNOULLI_QK and
+ *            SANTA_TWO_PASS
  *  seed      Philox4x64-10 key word 0 (ignored for SANTA_DENSE, except for the ternary
  *            query draws of SANTA_BERNOULLI_QK)
  *  out       device fp32 [B, H_q, d] (bf16 with SANTA_OUT_BF16); n_b = 0 gives zeros
@@ -141,10 +153,11 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache,
 
 /*
  * santa_call_info -- *launches = the kernel launches one santa_decode call with this
- * shape, S and mode enqueues (for sizing CUDA graphs and counting work): the score stage
- * and the value stage (or the dense kernel and its merge), plus the ternary query draw of
- * SANTA_BERNOULLI_QK.  Host only.  Returns SANTA_OK or the argument errors of
- * santa_decode.
+ * shape, S and mode enqueues on the current device (for sizing CUDA graphs and counting
+ * work): 1 for the single-pass cluster kernel, else 2 (the score and value stages, or
+ * the dense kernel and its merge), plus 1 for the ternary query draw of
+ * SANTA_BERNOULLI_QK.  Reads device attributes; enqueues nothing.  Returns SANTA_OK or
+ * the argument errors of santa_decode.
  */
 int santa_call_info(const santa_shape *shape, int32_t S, int32_t mode, int32_t *launches);
 

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "../../include/santa.h"
+#include "santa_cluster.cuh"
 #include "santa_dense.cuh"
 #include "santa_gather.cuh"
 #include "santa_kernels.h"
@@ -28,6 +29,11 @@ int gather_smem_bytes(int D, int G, int S, int nch_used, int mode, bool xdedup)
 int dense_smem_bytes(int D, int G, int B)
 {
     return dense_smem(D, G, B).total;
+}
+
+int cluster_smem_bytes(int D, int G, int LW, int S, int mode, int C, int ns)
+{
+    return cluster_smem(D, G, LW, S, mode, C, ns).total;
 }
 
 
@@ -210,7 +216,8 @@ int check_shape(const santa_shape *sh)
 
 int check_mode_S(int32_t mode_flags, int32_t S)
 {
-    if (mode_flags & ~(0xff | SANTA_GROUP_DEDUP | SANTA_OUT_BF16 | SANTA_BERNOULLI_QK)) return SANTA_ERR_INVALID_ARG;
+    if (mode_flags & ~(0xff | SANTA_GROUP_DEDUP | SANTA_OUT_BF16 | SANTA_BERNOULLI_QK | SANTA_TWO_PASS))
+        return SANTA_ERR_INVALID_ARG;
     const int mode = mode_flags & 0xff;
     if (mode < SANTA_DENSE || mode > SANTA_IID) return SANTA_ERR_INVALID_ARG;
     if (mode != SANTA_DENSE && (S < 1 || S > SMAX)) return SANTA_ERR_INVALID_ARG;
@@ -272,6 +279,87 @@ int make_map_bf16(CUtensorMap *map, const void *base, int D, long long rows, int
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? SANTA_OK : SANTA_ERR_CUDA;
+}
+
+// The single-pass cluster kernel, when it applies: one cluster of C CTAs per (b, KV head),
+// the largest C (at most 16) such that the B * H_kv clusters fit the GPU at once, each CTA
+// holding at most CL_LWMAX keys and the points of its group (G * S <= 2048) in shared
+// memory.  Otherwise (larger batches, longer caches) the score and value stages run as
+// two launches.
+struct ClusterPlan {
+    int C, LW, ns, smem;
+};
+
+struct ClusterOcc {
+    const void *fn;
+    int dev, C, smem, nclus;
+};
+ClusterOcc g_cocc[512];
+int g_ncocc = 0;
+
+// Clusters of C CTAs (smem bytes each) of kernel fn resident at once on device dev.
+int max_active_clusters(const void *fn, int dev, int C, int smem)
+{
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (int i = 0; i < g_ncocc; ++i)
+            if (g_cocc[i].fn == fn && g_cocc[i].dev == dev && g_cocc[i].C == C && g_cocc[i].smem == smem)
+                return g_cocc[i].nclus;
+    }
+    int occ = 0;
+    if (prepare_fn(fn, dev, smem, CL_NT, &occ)) return 0;
+    if (C > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)C);
+    cfg.blockDim = dim3(CL_NT);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int nclus = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclus, fn, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        nclus = 0;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_ncocc < 512) g_cocc[g_ncocc++] = ClusterOcc{fn, dev, C, smem, nclus};
+    return nclus;
+}
+
+bool plan_cluster(const santa_shape *shape, int S, int32_t mode_flags, int dev, int sms, int optin, ClusterPlan *pl)
+{
+    const int mode = mode_flags & 0xff;
+    if (mode == SANTA_DENSE || (mode_flags & (SANTA_GROUP_DEDUP | SANTA_TWO_PASS))) return false;
+    const int D = shape->d, G = shape->H_q / shape->H_kv;
+    const long long groups = (long long)shape->B * shape->H_kv;
+    if (G * S > 2048 || groups > sms) return false;
+    const void *fn = (D == 128) ? kernel_d128(KIND_CLUSTER, G) : kernel_d64(KIND_CLUSTER, G);
+    if (!fn) return false;
+    const int units = (shape->n_max + SC_M - 1) / SC_M;
+    for (int C = (int)(sms / groups < CL_MAXC ? sms / groups : CL_MAXC); C >= 1; --C) {
+        const int LW = (units + C - 1) / C * SC_M;
+        if (LW > CL_LWMAX) return false;  // (a smaller C only needs more keys per CTA)
+        int ns = cluster_max_stages(D), smem = 0;
+        for (; ns >= cluster_min_stages(D); --ns) {
+            smem = cluster_smem_bytes(D, G, LW, S, mode, C, ns);
+            if (smem <= optin) break;
+        }
+        if (ns < cluster_min_stages(D)) return false;
+        if (max_active_clusters(fn, dev, C, smem) < groups) continue;
+        pl->C = C;
+        pl->LW = LW;
+        pl->ns = ns;
+        pl->smem = smem;
+        return true;
+    }
+    return false;
 }
 
 }  // namespace
@@ -398,6 +486,41 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     const unsigned long long wlim = g_wait_limit_ns.load(std::memory_order_relaxed);
     p.wait_ns = wlim ? wlim : 2000000000ull;
 
+    ClusterPlan cp{};
+    const bool single = plan_cluster(shape, p.S, mode_flags, dev, sms, optin, &cp);
+    if (single) {
+        // one launch: the single-pass cluster kernel (keys per CTA in Params::L)
+        const void *fc = (D == 128) ? kernel_d128(KIND_CLUSTER, G) : kernel_d64(KIND_CLUSTER, G);
+        p.L = cp.LW;
+        p.nstages = cp.ns;
+        const long long krows = (long long)shape->B * shape->H_kv * shape->n_max;
+        CUtensorMap tm_k, tm_kt, tm_q;
+        if ((rc = make_map_bf16(&tm_k, k_cache, D, krows, SC_M))) return rc;
+        if ((rc = make_map_bf16(&tm_kt, k_cache, D, krows, SC_BOX_ROWS))) return rc;
+        if ((rc = make_map_bf16(&tm_q, q, D, (long long)shape->B * shape->H_q, G))) return rc;
+        if (ternary) {
+            const int BH = shape->B * shape->H_q;
+            santa_ternary_kernel<<<(unsigned)((BH + 7) / 8), 256, 0, (cudaStream_t)stream>>>(
+                BH, shape->H_q, shape->d, seed, static_cast<const uint16_t *>(q_user),
+                reinterpret_cast<uint16_t *>(ws + wl.qt));
+            if (cudaGetLastError() != cudaSuccess) return SANTA_ERR_CUDA;
+        }
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)((long long)shape->B * shape->H_kv * cp.C));
+        cfg.blockDim = dim3(CL_NT);
+        cfg.dynamicSmemBytes = (size_t)cp.smem;
+        cfg.stream = (cudaStream_t)stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)cp.C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        void *cargs[] = {&p, &tm_k, &tm_kt, &tm_q};
+        if (cudaLaunchKernelExC(&cfg, fc, cargs) != cudaSuccess) return SANTA_ERR_CUDA;
+        return SANTA_OK;
+    }
     const int kind = dense ? KIND_DENSE : KIND_SCORE;
     const void *fn = (D == 128) ? kernel_d128(kind, G) : kernel_d64(kind, G);
     if (!fn) return SANTA_ERR_UNSUPPORTED;
@@ -499,7 +622,11 @@ int santa_call_info(const santa_shape *shape, int32_t S, int32_t mode, int32_t *
     if (rc) return rc;
     if ((rc = check_mode_S(mode, S))) return rc;
     if (!launches) return SANTA_ERR_INVALID_ARG;
-    *launches = 2 + ((mode & SANTA_BERNOULLI_QK) ? 1 : 0);
+    int dev, sms, optin;
+    if ((rc = device_info(&dev, &sms, &optin))) return rc;
+    ClusterPlan cp{};
+    const bool single = plan_cluster(shape, (mode & 0xff) == SANTA_DENSE ? 1 : S, mode, dev, sms, optin, &cp);
+    *launches = (single ? 1 : 2) + ((mode & SANTA_BERNOULLI_QK) ? 1 : 0);
     return SANTA_OK;
 }
 

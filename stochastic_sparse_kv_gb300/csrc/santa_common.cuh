@@ -87,6 +87,7 @@ struct Params {
     int L;            // keys per work unit (sampled path) or split length (dense), multiple of 64
     int S, mode;
     int xdedup;       // value stage: the group's heads share V loads (thread-block clusters)
+    int nstages;      // single-pass cluster kernel: stages of its ring
     int out_bf16;     // out is bf16 (each fp32 result rounded once), else fp32
     uint64_t seed;
     double rS;        // fp64 value nearest 1/S

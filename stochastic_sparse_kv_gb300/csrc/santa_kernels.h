@@ -4,7 +4,7 @@
 
 namespace santa {
 
-enum KernelKind : int { KIND_SCORE = 0, KIND_DENSE = 1, KIND_GATHER = 2, KIND_DMERGE = 3 };
+enum KernelKind : int { KIND_SCORE = 0, KIND_DENSE = 1, KIND_GATHER = 2, KIND_DMERGE = 3, KIND_CLUSTER = 4 };
 
 // Kernel entry for (kind, G) at head dimension 64 or 128, or nullptr.
 const void *kernel_d64(int kind, int G);
@@ -14,6 +14,7 @@ const void *kernel_d128(int kind, int G);
 int score_smem_bytes(int D, int G, int B);
 int gather_smem_bytes(int D, int G, int S, int nch_used, int mode, bool xdedup);
 int dense_smem_bytes(int D, int G, int B);
+int cluster_smem_bytes(int D, int G, int LW, int S, int mode, int C, int ns);
 
 // Device points kernel (santa_sample_points).
 const void *points_kernel();

@@ -1,4 +1,5 @@
 // Kernel instantiations for head dimension 64.
+#include "santa_cluster.cuh"
 #include "santa_dense.cuh"
 #include "santa_gather.cuh"
 #include "santa_kernels.h"
@@ -14,6 +15,15 @@ const void *kernel_d64(int kind, int G)
         case 2: return (const void *)santa_gather_kernel<64, 2>;
         case 4: return (const void *)santa_gather_kernel<64, 4>;
         case 8: return (const void *)santa_gather_kernel<64, 8>;
+        }
+        return nullptr;
+    }
+    if (kind == KIND_CLUSTER) {  // the single-pass kernel for small batches (thread-block clusters)
+        switch (G) {
+        case 1: return (const void *)santa_cluster_kernel<64, 1>;
+        case 2: return (const void *)santa_cluster_kernel<64, 2>;
+        case 4: return (const void *)santa_cluster_kernel<64, 4>;
+        case 8: return (const void *)santa_cluster_kernel<64, 8>;
         }
         return nullptr;
     }

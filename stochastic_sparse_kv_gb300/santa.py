@@ -21,6 +21,7 @@ MODES = {"dense": DENSE, "stratified": STRATIFIED, "systematic": SYSTEMATIC, "ii
 GROUP_DEDUP = 0x100  # or-ed into a sampling mode: V rows loaded once per KV-head group
 OUT_BF16 = 0x200     # or-ed into any mode: out is bf16 (the fp32 result rounded once)
 BERNOULLI_QK = 0x400  # or-ed into any mode: score with each head's ternary query draw
+TWO_PASS = 0x800      # or-ed into a sampling mode: never the single-pass cluster kernel
 DEV_BAD_SEQLEN, DEV_TIMEOUT = 1, 2
 
 # every symbol include/santa.h declares
@@ -139,13 +140,14 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_le
            S: int, mode="systematic", seed: int = 0, scale: float = 0.0, out: torch.Tensor | None = None,
            idx_out: torch.Tensor | None = None, want_idx: bool = True, workspace: torch.Tensor | None = None,
            stream=None, group_dedup: bool = False, out_dtype: torch.dtype = torch.float32,
-           bernoulli: bool = False):
+           bernoulli: bool = False, two_pass: bool = False):
     """One SANTA (or dense) decode step on the GPU.  q [B,H_q,d], k/v [B,H_kv,n_max,d] bf16,
     seq_lens [B] int32, all on one CUDA device.  Returns (out [B,H_q,d], idx int32
     [B,H_q,S] or None).  out is fp32, or bf16 (SANTA_OUT_BF16) when `out` is a bf16 tensor
     or out_dtype is torch.bfloat16.  group_dedup: load each sampled V row once per group of
     query heads sharing a KV head (SANTA_GROUP_DEDUP).  bernoulli: score with each head's
-    ternary query draw (SANTA_BERNOULLI_QK)."""
+    ternary query draw (SANTA_BERNOULLI_QK).  two_pass: the score and value stages as two
+    launches even where the single-pass cluster kernel applies (SANTA_TWO_PASS)."""
     m = _mode(mode)
     B, H_q, d = q.shape
     _, H_kv, n_max, d2 = k_cache.shape
@@ -167,7 +169,7 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_le
     nbytes = workspace_size(shape, S if m != DENSE else 1, m)
     ws = workspace if workspace is not None else _cached_workspace(nbytes, dev, stream)
     mf = m | (GROUP_DEDUP if (group_dedup and m != DENSE) else 0) | (OUT_BF16 if out.dtype == torch.bfloat16 else 0) \
-        | (BERNOULLI_QK if bernoulli else 0)
+        | (BERNOULLI_QK if bernoulli else 0) | (TWO_PASS if (two_pass and m != DENSE) else 0)
     rc = load().santa_decode(ctypes.byref(shape), ctypes.c_void_p(q.data_ptr()),
                              ctypes.c_void_p(k_cache.data_ptr()), ctypes.c_void_p(v_cache.data_ptr()),
                              ctypes.c_void_p(seq_lens.data_ptr()), int(S), mf, ctypes.c_uint64(seed),
@@ -187,11 +189,11 @@ class DecodePlan:
     def __init__(self, q, k_cache, v_cache, seq_lens, S: int, mode="systematic", scale: float = 0.0,
                  out: torch.Tensor | None = None, idx_out: torch.Tensor | None = None, want_idx: bool = True,
                  workspace: torch.Tensor | None = None, stream=None, group_dedup: bool = False,
-                 out_dtype: torch.dtype = torch.float32, bernoulli: bool = False):
+                 out_dtype: torch.dtype = torch.float32, bernoulli: bool = False, two_pass: bool = False):
         m = _mode(mode)
         # one checked call through decode() fixes every buffer (and runs the step once)
         self.out, self.idx_out = decode(q, k_cache, v_cache, seq_lens, S, m, 0, scale, out, idx_out, want_idx,
-                                        workspace, stream, group_dedup, out_dtype, bernoulli)
+                                        workspace, stream, group_dedup, out_dtype, bernoulli, two_pass)
         B, H_q, d = q.shape
         _, H_kv, n_max, _ = k_cache.shape
         self._shape = make_shape(B, H_q, H_kv, d, n_max, scale)
@@ -200,7 +202,8 @@ class DecodePlan:
         # the buffers (and the stream object, if one was given) stay alive with the plan
         self._keep = (q, k_cache, v_cache, seq_lens, ws, stream)
         flags = m | (GROUP_DEDUP if (group_dedup and m != DENSE) else 0) | \
-            (OUT_BF16 if self.out.dtype == torch.bfloat16 else 0) | (BERNOULLI_QK if bernoulli else 0)
+            (OUT_BF16 if self.out.dtype == torch.bfloat16 else 0) | (BERNOULLI_QK if bernoulli else 0) | \
+            (TWO_PASS if (two_pass and m != DENSE) else 0)
         vp = ctypes.c_void_p
         self._fn = load().santa_decode
         self._pre = (ctypes.byref(self._shape), vp(q.data_ptr()), vp(k_cache.data_ptr()), vp(v_cache.data_ptr()),
@@ -216,10 +219,12 @@ class DecodePlan:
         return self.out, self.idx_out
 
 
-def call_info(shape: Shape, S: int, mode, group_dedup: bool = False, bernoulli: bool = False) -> int:
+def call_info(shape: Shape, S: int, mode, group_dedup: bool = False, bernoulli: bool = False,
+              two_pass: bool = False) -> int:
     """santa_call_info: the kernel launches one decode call with this shape, S and mode
-    enqueues."""
-    m = _mode(mode) | (GROUP_DEDUP if group_dedup else 0) | (BERNOULLI_QK if bernoulli else 0)
+    enqueues on the current device (1: the single-pass cluster kernel)."""
+    m = _mode(mode) | (GROUP_DEDUP if group_dedup else 0) | (BERNOULLI_QK if bernoulli else 0) | \
+        (TWO_PASS if two_pass else 0)
     n = ctypes.c_int32(0)
     _check(load().santa_call_info(ctypes.byref(shape), int(S), m, ctypes.byref(n)), "santa_call_info")
     return int(n.value)

@@ -64,7 +64,8 @@ def test_workspace_size_matches_layout(lib):
     ((1, 32, 8, 128, 1024), 16, 0x302, 0),      # both flags
     ((1, 32, 8, 128, 1024), 16, 0x402, 0),      # SANTA_BERNOULLI_QK is a valid flag
     ((1, 32, 8, 128, 1024), 16, 0x400, 0),      # ... also with the dense mode
-    ((1, 32, 8, 128, 1024), 16, 0x802, -1),     # unknown flag bits
+    ((1, 32, 8, 128, 1024), 16, 0x802, 0),      # SANTA_TWO_PASS is a valid flag
+    ((1, 32, 8, 128, 1024), 16, 0x1002, -1),    # unknown flag bits
     ((1025, 32, 8, 128, 1024), 16, 2, -4),      # B > 1024
     ((1, 32, 8, 128, 524289), 16, 2, -4),       # n_max too large
     ((1024, 8, 8, 64, 262144), 16, 2, -4),      # B*H_kv*n_max = 2^31 cache rows: past 32-bit copy coordinates
@@ -109,8 +110,7 @@ def test_decode_rejects_bad_arguments_on_the_host(lib):
     assert lib.santa_call_info(ctypes.byref(bad), 16, 2, ctypes.byref(n)) == -1
     assert lib.santa_call_info(ctypes.byref(sh), 0, 2, ctypes.byref(n)) == -1
     assert lib.santa_call_info(ctypes.byref(sh), 16, 2, None) == -1
-    assert lib.santa_call_info(ctypes.byref(sh), 16, 2, ctypes.byref(n)) == 0 and n.value == 2
-    assert lib.santa_call_info(ctypes.byref(sh), 16, 0x402, ctypes.byref(n)) == 0 and n.value == 3
+    assert lib.santa_call_info(ctypes.byref(sh), 16, 0x1002, ctypes.byref(n)) == -1
     assert lib.santa_ternary_query(1, 1, 96, ctypes.c_void_p(good), ctypes.c_uint64(0), ctypes.c_void_p(good),
                                    None) == -4
     assert lib.santa_ternary_query(1, 1, 128, ctypes.c_void_p(good + 2), ctypes.c_uint64(0),

@@ -417,11 +417,36 @@ def test_bernoulli_qk_llama_b1_32k():
                   f"ternary density {nnz.mean() / w.d:.3f}")
 
 
-# ------------------------------------------------------------------ launch count
+# ------------------------------------------------------------------ single pass vs two launches
+
+@pytest.mark.parametrize("case", CASES)
+@pytest.mark.parametrize("mode", ["systematic", "stratified", "iid"])
+def test_single_pass_matches_two_launches(case, mode):
+    """Where the single-pass cluster kernel applies (the default for small problems), it
+    computes the same CDF arithmetic as the two launches of the score and value stages:
+    identical indices; outputs equal up to the order of the gather's fp32 additions."""
+    d, H_q, H_kv, n_max, seq, S = case
+    w, q, k, v, sl = workloads.small("sp", len(seq), H_q, H_kv, d, n_max, S, seq_lens=seq, seed=d + H_q + n_max)
+    shape = santa.make_shape(len(seq), H_q, H_kv, d, n_max)
+    assert santa.call_info(shape, S, mode, two_pass=True) == 2
+    qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
+    for seed in (3, 4):
+        o1, i1 = santa.decode(qd, kd, vd, sld, S, mode, seed=seed)
+        o2, i2 = santa.decode(qd, kd, vd, sld, S, mode, seed=seed, two_pass=True)
+        torch.cuda.synchronize()
+        assert torch.equal(i1, i2)
+        assert (o1 - o2).abs().max().item() <= 1e-5
+
 
 def test_call_info_counts_the_launches_of_a_call():
-    sh = santa.make_shape(16, 32, 8, 128, 32768)
-    assert santa.call_info(sh, 256, "systematic") == 2
-    assert santa.call_info(sh, 256, "stratified", bernoulli=True) == 3
-    assert santa.call_info(sh, 256, "systematic", group_dedup=True) == 2
-    assert santa.call_info(sh, 1, "dense") == 2
+    big = santa.make_shape(16, 32, 8, 128, 32768)
+    assert santa.call_info(big, 256, "systematic") == 2
+    assert santa.call_info(big, 256, "stratified", bernoulli=True) == 3
+    assert santa.call_info(big, 1, "dense") == 2
+    one = santa.make_shape(1, 32, 8, 128, 32768)   # B=1, 32k keys: the single-pass kernel
+    assert santa.call_info(one, 256, "systematic") == 1
+    assert santa.call_info(one, 256, "iid", bernoulli=True) == 2
+    assert santa.call_info(one, 256, "systematic", two_pass=True) == 2
+    assert santa.call_info(one, 256, "systematic", group_dedup=True) == 2
+    assert santa.call_info(santa.make_shape(4, 32, 8, 128, 8192), 256, "stratified") == 1
+    assert santa.call_info(santa.make_shape(4, 32, 8, 128, 32768), 256, "systematic") == 2

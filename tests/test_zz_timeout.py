@@ -15,28 +15,31 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.mark.parametrize("mode", ["systematic", "dense"])
-def test_short_wait_limit_reports_a_timeout_and_leaves_the_context_usable(mode):
-    seq = [16384, 16384, 9000, 16384]
-    _, q, k, v, sl = workloads.small("timeout", 4, 32, 8, 128, 16384, 256, seq_lens=seq, seed=31)
+@pytest.mark.parametrize("mode,B,two_pass", [("systematic", 4, True), ("dense", 4, False), ("systematic", 1, False)])
+def test_short_wait_limit_reports_a_timeout_and_leaves_the_context_usable(mode, B, two_pass):
+    """(two_pass: the score and value stages as two launches; B=1: the single-pass cluster
+    kernel, whose CTAs all still reach every cluster barrier after their waits give up)"""
+    seq = [16384, 16384, 9000, 16384][:B]
+    _, q, k, v, sl = workloads.small("timeout", B, 32, 8, 128, 16384, 256, seq_lens=seq, seed=31)
     qd, kd, vd, sld = q.to(DEV), k.to(DEV), v.to(DEV), sl.to(DEV)
-    shape = santa.make_shape(4, 32, 8, 128, 16384)
+    shape = santa.make_shape(B, 32, 8, 128, 16384)
+    assert santa.call_info(shape, 256, mode, two_pass=two_pass) == (1 if B == 1 else 2)
     ws = santa.new_workspace(santa.workspace_size(shape, 256, mode), DEV)
-    ref, iref = santa.decode(qd, kd, vd, sld, 256, mode, seed=3, workspace=ws)
+    ref, iref = santa.decode(qd, kd, vd, sld, 256, mode, seed=3, workspace=ws, two_pass=two_pass)
     ref = ref.clone()
     iref = iref.clone() if iref is not None else None
     torch.cuda.synchronize()
     assert santa.device_status(ws) == 0
     try:
         santa.set_wait_limit(1)  # 1 ns: the first wait that is not already satisfied gives up
-        santa.decode(qd, kd, vd, sld, 256, mode, seed=3, workspace=ws)
+        santa.decode(qd, kd, vd, sld, 256, mode, seed=3, workspace=ws, two_pass=two_pass)
         torch.cuda.synchronize()
         code = santa.device_status(ws)
     finally:
         santa.set_wait_limit(0)
     assert code & santa.DEV_TIMEOUT
     assert santa.device_status(ws) == 0  # cleared by the read
-    out, idx = santa.decode(qd, kd, vd, sld, 256, mode, seed=3, workspace=ws)
+    out, idx = santa.decode(qd, kd, vd, sld, 256, mode, seed=3, workspace=ws, two_pass=two_pass)
     torch.cuda.synchronize()
     assert santa.device_status(ws) == 0
     assert torch.equal(out, ref)
