@@ -240,6 +240,19 @@ int santa_decode_static(const santa_shape *shape, const void *q, const void *k_c
                         const void *v_cache, const int32_t *seq_lens, int32_t S, int32_t mode,
                         uint64_t seed, float *out, int32_t *idx_out, void *stream);
 
+/*
+ * santa_timeline_buffer -- for reading where a call's time goes: in a library built with
+ * -DSANTA_TIMELINE (libsanta_timeline.so; stochastic_sparse_kv_gb300/timeline.py builds
+ * and reads it), later calls write %globaltimer stamps (ns) into buf, a device buffer of
+ * at least 16 * 8 * (1024 + B * H_q) bytes: 16 stamps per row, one row per CTA of the score
+ * or single-pass kernel (rows 0..1023) and per value-stage CTA (row 1024 + b * H_q + h).
+ * Rows beyond `bytes` are not written.  buf = NULL stops it.  Errors: INVALID_ARG when
+ * bytes hold fewer than 1024 rows, MISALIGNED when buf is not 8-byte aligned.  The normal
+ * build has no stamps and returns SANTA_ERR_UNSUPPORTED.
+ * Not for production use: the buffer is shared by every later call, process-wide.
+ */
+int santa_timeline_buffer(void *buf, size_t bytes);
+
 /* santa_status_string -- static description of a status code. */
 const char *santa_status_string(int status);
 

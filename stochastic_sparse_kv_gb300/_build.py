@@ -15,7 +15,9 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsanta.so")
 UNITS = ["santa_api.cu", "santa_kernels_d128.cu", "santa_kernels_d64.cu"]
 HEADERS = ["santa_common.cuh", "santa_sample.cuh", "santa_tcgen05.cuh", "santa_score.cuh", "santa_gather.cuh", "santa_dense.cuh",
-           "santa_kernels.h"]
+           "santa_cluster.cuh", "santa_kernels.h"]
+# the timeline build: the same sources with %globaltimer stamps (santa_timeline_buffer)
+TIMELINE_LIB = os.path.join(HERE, "libsanta_timeline.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
@@ -35,17 +37,20 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, timeline: bool = False) -> str:
+    """Build libsanta.so (timeline=True: libsanta_timeline.so, compiled with -DSANTA_TIMELINE
+    into its own object folder); returns the library's path."""
+    out_dir, lib, extra = (OUT_DIR + "_timeline", TIMELINE_LIB, ["-DSANTA_TIMELINE"]) if timeline else (OUT_DIR, LIB, [])
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "santa.h")]
     objs, jobs = [], []
     for u in UNITS:
         src = os.path.join(CSRC, u)
-        obj = os.path.join(OUT_DIR, u.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, u.replace(".cu", ".o"))
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
-            cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+            cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
             if ptxas_v:
                 cmd.insert(1, "-Xptxas=-v")
             jobs.append(cmd)
@@ -61,13 +66,12 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
                     sys.stderr.write(r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError("nvcc failed: " + " ".join(cmd))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True, ptxas_v="-v" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_v="-v" in sys.argv, timeline="--timeline" in sys.argv))

@@ -132,6 +132,8 @@ const void *points_iid_kernel() { return (const void *)santa_points_iid_kernel; 
 constexpr int MAX_DEV_STATIC = 64;
 std::mutex g_static_mu;
 std::atomic<unsigned long long> g_wait_limit_ns{0};  // 0: the default of 2 s
+std::atomic<unsigned long long *> g_timeline{nullptr};  // SANTA_TIMELINE builds: stamp buffer
+std::atomic<int> g_timeline_rows{0};
 
 namespace {
 
@@ -485,6 +487,8 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     p.tau2 = (float)(3.0 * 1.4426950408889634);  // re-score keys within e^-3 of the maximum
     const unsigned long long wlim = g_wait_limit_ns.load(std::memory_order_relaxed);
     p.wait_ns = wlim ? wlim : 2000000000ull;
+    p.tl = g_timeline.load(std::memory_order_relaxed);
+    p.tl_rows = p.tl ? g_timeline_rows.load(std::memory_order_relaxed) : 0;
 
     ClusterPlan cp{};
     const bool single = plan_cluster(shape, p.S, mode_flags, dev, sms, optin, &cp);
@@ -628,6 +632,22 @@ int santa_call_info(const santa_shape *shape, int32_t S, int32_t mode, int32_t *
     const bool single = plan_cluster(shape, (mode & 0xff) == SANTA_DENSE ? 1 : S, mode, dev, sms, optin, &cp);
     *launches = (single ? 1 : 2) + ((mode & SANTA_BERNOULLI_QK) ? 1 : 0);
     return SANTA_OK;
+}
+
+int santa_timeline_buffer(void *buf, size_t bytes)
+{
+#ifdef SANTA_TIMELINE
+    if (buf && bytes < (size_t)16 * 8 * TL_VALUE_ROW0) return SANTA_ERR_INVALID_ARG;
+    if (buf && !aligned(buf, 8)) return SANTA_ERR_MISALIGNED;
+    const size_t rows = bytes / (16 * 8);
+    g_timeline_rows.store(buf ? (int)std::min<size_t>(rows, 1u << 30) : 0, std::memory_order_relaxed);
+    g_timeline.store(static_cast<unsigned long long *>(buf), std::memory_order_relaxed);
+    return SANTA_OK;
+#else
+    (void)buf;
+    (void)bytes;
+    return SANTA_ERR_UNSUPPORTED;
+#endif
 }
 
 int santa_set_wait_limit(uint64_t limit_ns)

@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(CL_NT, 1)
     uint64_t *zs = reinterpret_cast<uint64_t *>(misc + 48);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float NEG_INF = __int_as_float(0xff800000);
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 0);
 
     int n = p.seq_lens[b];
     if (n < 0 || n > p.n_max) {
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(CL_NT, 1)
     // shared memory, makes sure that every CTA of the cluster has started
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 1);
     if (warp == SC_WARP_PROD) {
         // ================= producer: this CTA's units of the group, in order
         if (lane == 0) {
@@ -260,6 +262,7 @@ __global__ void __launch_bounds__(CL_NT, 1)
                     tma_load_2d_plain(qst + (s * NH + hf) * QB, &tm_q, hf * 64, grp * G, &full[s]);
             }
             tmem_slot[2] = (uint32_t)i;
+            SANTA_STAMP(blockIdx.x, 2);
         }
         __syncwarp();
     } else if (warp == SC_WARP_MMA) {
@@ -426,6 +429,7 @@ __global__ void __launch_bounds__(CL_NT, 1)
     // the value stage's scratch, once the fills still in flight (after a timeout) have landed
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 3);
     if (warp == SC_WARP_PROD && lane == 0) {
         const int nfill = (int)tmem_slot[2];
         for (int f = (int)tmem_slot[1]; f < nfill; ++f)
@@ -437,6 +441,7 @@ __global__ void __launch_bounds__(CL_NT, 1)
     }
     __syncthreads();
 
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 4);
     // ================= value stage: every thread of the CTA
     if (tid < G) {
         misc[tid] = INT_MIN;      // below the key of every fp32 value
@@ -446,6 +451,7 @@ __global__ void __launch_bounds__(CL_NT, 1)
     }
     __syncthreads();
 
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 5);
     // 1. this CTA's maximum and largest scale per head, to every CTA of the cluster
     for (int i = tid; i < G * ncl; i += CL_NT) {
         const int h = i / ncl, c = i % ncl;
@@ -471,6 +477,7 @@ __global__ void __launch_bounds__(CL_NT, 1)
     }
     __syncthreads();
 
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 6);
     // 2. fixed-point chunk totals in the head's scale 2^-C; hot chunks (maximum >= M - tau2)
     for (int i = tid; i < G * ncl; i += CL_NT) {
         const int h = i / ncl, c = i % ncl;
@@ -533,6 +540,7 @@ __global__ void __launch_bounds__(CL_NT, 1)
     }
     __syncthreads();
 
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 7);
     // 3. exclusive prefix of this CTA's chunks per head (one warp per head, up to four
     //    consecutive chunks per lane); the range total to every CTA of the cluster
     if (warp < G) {
@@ -576,6 +584,7 @@ __global__ void __launch_bounds__(CL_NT, 1)
     }
     __syncthreads();
 
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 8);
     // 4. the points of each head that fall in this CTA's mass range: T = t Z, then
     //    i = min{ j : W_j > T } by chunk (binary search on the prefix) and key (the chunk's
     //    weights), both in shared memory
@@ -630,6 +639,7 @@ __global__ void __launch_bounds__(CL_NT, 1)
     }
     __syncthreads();
 
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 9);
     // 5. the distinct V rows of this CTA's points (first occurrences, in point order; a key's
     //    points all land in this CTA, in one run), one warp per head: lead[h][k] = the k-th
     //    first occurrence, lead[G S + h] = their number, lead[G S + G + h] = 1 + the last point
@@ -702,6 +712,7 @@ __global__ void __launch_bounds__(CL_NT, 1)
         }
     }
     __syncthreads();
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 10);
     //    slice k (dimensions [k DS, (k+1) DS)) of every head's partial sums to CTA k
     const int DS = (D + C - 1) / C;
     if (DS % 4 == 0) {
@@ -725,6 +736,7 @@ __global__ void __launch_bounds__(CL_NT, 1)
         for (int k = 0; k < C; ++k) sum = __fadd_rn(sum, xpart[(k * G + h) * DS + e]);
         store_out(p, ((size_t)grp * G + h) * D + rk * DS + e, __fdiv_rn(sum, (float)S));
     }
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 11);
 }
 
 }  // namespace santa

@@ -94,7 +94,23 @@ struct Params {
     float k2_hi, k2_lo;  // scale*log2(e) as an unevaluated fp32 sum
     float tau2;       // re-scoring window below the maximum (log2 units)
     uint64_t wait_ns; // bounded-wait limit of the main loops (santa_set_wait_limit)
+    unsigned long long *tl;  // timeline stamps (a build with SANTA_TIMELINE only; else NULL)
+    int tl_rows;             // rows of 16 stamps that tl holds
 };
+
+// Timeline of a call, for reading where the time goes: a build with -DSANTA_TIMELINE
+// (libsanta_timeline.so, see timeline.py) writes %globaltimer stamps into Params::tl,
+// 16 per row: score kernel and cluster kernel CTAs in rows [0, 1024), value-stage CTAs in
+// rows 1024 + (b * H_q + h).  The normal build compiles the stamps out.
+#ifdef SANTA_TIMELINE
+#define SANTA_STAMP(row, col)                                                                        \
+    do {                                                                                             \
+        if (p.tl && (int)(row) < p.tl_rows) p.tl[(size_t)(row) * 16 + (col)] = globaltimer_ns();     \
+    } while (0)
+#else
+#define SANTA_STAMP(row, col) ((void)0)
+#endif
+constexpr int TL_VALUE_ROW0 = 1024;
 
 // out[i] = v, as fp32 or rounded once to bf16 (round to nearest, ties to even).
 __device__ __forceinline__ void store_out(const Params &p, size_t i, float v)

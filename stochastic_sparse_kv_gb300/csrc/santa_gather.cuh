@@ -259,6 +259,7 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
     const int Cm = misc[GM_CMAX];
     const float thr = M - p.tau2;  // keys with a score >= thr are re-scored
 
+    if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 2);
     // ---- B. fixed-point chunk totals in the global scale; hot chunks (unordered list)
     int cnt = 0;
     for (int c = tid; c < nchn; c += NTH) {
@@ -307,6 +308,7 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
         team_sync<BAR, NTH>();
     }
 
+    if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 3);
     // ---- C. heavy keys of the hot chunks: slot q = hot entry * 8 + quarter (four keys,
     // one 16-byte load); up to eight loads in flight per thread before any is acted on,
     // so HCAP hot chunks take one round.
@@ -350,6 +352,7 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
     team_sync<BAR, NTH>();
     const int nhv = min(misc[GM_NHV], HKCAP);
 
+    if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 4);
     // ---- D. re-score the heavy keys (four lanes each) and patch their chunk totals
     for (int i0 = 0; i0 < nhv; i0 += NTH / 4) {  // (every lane runs every pass: they shuffle)
         const int i = i0 + tid / 4, part = tid & 3;
@@ -368,6 +371,7 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
     }
     team_sync<BAR, NTH>();
 
+    if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 5);
     // ---- E. exact exclusive prefix of the G_c: a contiguous range per thread
     {
         const int per = (nchn + NTH - 1) / NTH;
@@ -403,6 +407,7 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
     team_sync<BAR, NTH>();
     const uint64_t Z = scan64[NW];
 
+    if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 6);
     // ---- F. points -> chunk (binary search on O) -> key (the chunk's 32 weights, one line)
     for (int s = tid; s < S; s += NTH) {
         const uint64_t T = __umul64hi(tfx[s], Z);
@@ -443,6 +448,7 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
         if (D * 2 > 128) prefetch_l2(vrow + 64);
     }
     team_sync<BAR, NTH>();
+    if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 7);
     // The head's weights and chunk data have been read for the last time: drop them from
     // L2 so that they are never written back (the next step's score stage rewrites them).
     l2_discard_range(wrow, (size_t)nchn * CHUNK * sizeof(float), tid, NTH);
@@ -451,6 +457,7 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
     l2_discard_range(p.cmax + bhc, (size_t)p.nch * sizeof(float), tid, NTH);
     if (!in_smem) l2_discard_range(p.cpre + bhc, (size_t)p.nch * sizeof(uint64_t), tid, NTH);
 
+    if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 8);
     // ---- G. sorted indices out; each warp gathers the distinct rows of its run of
     // points (a row split between two warps is loaded by both, each with its own count)
     if (p.idx_out)
@@ -558,6 +565,7 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
                 for (int jj = 0; jj < G; ++jj) sum = __fadd_rn(sum, recv[jj * D + i]);
                 store_out(p, (size_t)bh * D + i, __fdiv_rn(sum, (float)S));
             }
+            if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 10);
             return;
         }
     }
@@ -610,12 +618,14 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc_s[(r0 * NPC + piece) * 8 + e] = acc[e];
         team_sync<BAR, NTH>();
+        if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 9);
         for (int i = tid; i < D; i += NTH) {
             float sum = 0.f;
             for (int r = 0; r < RSTEP; ++r) sum = __fadd_rn(sum, acc_s[(r * NPC + i / 8) * 8 + i % 8]);
             store_out(p, (size_t)bh * D + i, __fdiv_rn(sum, (float)S));
         }
     }
+    if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 10);
 }
 
 // One CTA per (b, h_q), a programmatic dependent of the score kernel (four CTAs per SM:
@@ -626,6 +636,7 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, bh = blockIdx.x;
+    if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 0);
     const int n = value_len(p, bh / p.H_q);
     if (n == 0) {  // (every CTA of a cluster shares b, so all of them leave here)
         value_empty<D, NT>(p, bh, tid);
@@ -635,6 +646,7 @@ __global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
     value_prologue<D, G, NT, 0>(p, bh, smem, lay, tid);
     pdl_wait();  // the score kernel's results are complete and visible from here on
     __syncthreads();
+    if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 1);
     if (p.xdedup)
         value_main<D, G, NT, 0, true>(p, bh, n, smem, lay, tid);
     else

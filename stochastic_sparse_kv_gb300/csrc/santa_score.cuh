@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(SC_NT, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 0);
 
     if (warp == SC_WARP_PROD) {
         // ================= producer: one thread streams K (and the group's queries)
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(SC_NT, 1)
                     tma_load_2d_plain(qst + (s * NH + hf) * QB, &tm_q, hf * 64, grp * G, &full[s]);
             }
             tmem_slot[2] = (uint32_t)i;
+            SANTA_STAMP(blockIdx.x, 1);
         }
         __syncwarp();
     } else if (warp == SC_WARP_MMA) {
@@ -434,6 +436,7 @@ __global__ void __launch_bounds__(SC_NT, 1)
     // timeout, fills the MMA thread never consumed get a bounded wait to land first.
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 2);
     if (warp == SC_WARP_PROD && lane == 0) {
         const int nfill = (int)tmem_slot[2];
         for (int f = (int)tmem_slot[1]; f < nfill; ++f)
@@ -446,6 +449,7 @@ __global__ void __launch_bounds__(SC_NT, 1)
     // The value stage is a programmatic dependent: let it launch only now (triggering at
     // the start measured ~9 us slower at B=16); it waits for the whole grid to complete.
     pdl_launch_dependents();
+    if (tid == 0) SANTA_STAMP(blockIdx.x, 3);
     if (tid == 0) {
         const int done = atomicAdd(p.ctrl + CTRL_EXIT, 1);
         if (done == (int)gridDim.x - 1) {

@@ -27,7 +27,7 @@ DEV_BAD_SEQLEN, DEV_TIMEOUT = 1, 2
 # every symbol include/santa.h declares
 EXPORTS = ("santa_workspace_size", "santa_workspace_init", "santa_decode", "santa_sample_points",
            "santa_device_status", "santa_status_string", "santa_version", "santa_decode_static",
-           "santa_set_wait_limit", "santa_ternary_query", "santa_call_info")
+           "santa_set_wait_limit", "santa_ternary_query", "santa_call_info", "santa_timeline_buffer")
 ERR_DEVICE = -6
 ERR_SCRATCH = -7
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -46,14 +46,18 @@ class Shape(ctypes.Structure):
 
 _lock = threading.Lock()
 _lib = None
+_lib_path = None
 
 
 def load(path: str | None = None):
     """Load libsanta.so (raises if it is missing: build it with __graft_entry__.build()).
-    The SANTA_LIBRARY environment variable, if set, names another build to load."""
-    global _lib
+    The SANTA_LIBRARY environment variable, if set, names another build to load; so does
+    `path`, on the first call of a process (one build per process)."""
+    global _lib, _lib_path
     with _lock:
         if _lib is not None:
+            if path is not None and os.path.realpath(path) != _lib_path:
+                raise RuntimeError(f"{_lib_path} is loaded already; one libsanta build per process")
             return _lib
         p = path or os.environ.get("SANTA_LIBRARY", LIB_PATH)
         if not os.path.exists(p):
@@ -79,11 +83,13 @@ def load(path: str | None = None):
         lib.santa_ternary_query.restype = ctypes.c_int
         lib.santa_call_info.argtypes = [ctypes.POINTER(Shape), i32, i32, ctypes.POINTER(i32)]
         lib.santa_call_info.restype = ctypes.c_int
+        lib.santa_timeline_buffer.argtypes = [vp, sz]
+        lib.santa_timeline_buffer.restype = ctypes.c_int
         lib.santa_set_wait_limit.argtypes = [u64]
         lib.santa_set_wait_limit.restype = ctypes.c_int
         lib.santa_version.argtypes = []
         lib.santa_version.restype = ctypes.c_int
-        _lib = lib
+        _lib, _lib_path = lib, os.path.realpath(p)
         return lib
 
 
