@@ -67,12 +67,31 @@ __host__ __device__ inline GatherSmem gather_smem(int D, int G, int S, int nch_u
     s.hvw = off; off = (int)align_up((size_t)off + HKCAP * 4, 16);
     s.hist = off; off = (int)align_up((size_t)off + HBINS * 4, 16);
     s.idx = off; off = (int)align_up((size_t)off + Sp * 4, 16);
-    s.lead = off; off = (int)align_up((size_t)off + (S + 1) * 4, 16);
-    s.acc = off; off += nth * 8 * 4;  // per-thread partial sums of the gather (8 dims each)
+    // G's arrays overlay what F read for the last time, so that four CTAs fit on an SM up to
+    // S = 2048: the distinct-row list over the points ((S + 1) * 4 <= S * 8 bytes), the
+    // per-thread partial sums of the gather (8 dims each) over the chunk arrays, when these
+    // are large enough
+    s.lead = s.t;
+    const int accb = nth * 8 * 4;
+    if (s.hot - s.O >= accb) {
+        s.acc = s.O;
+    } else {
+        s.acc = off;
+        off += accb;
+    }
     s.qf = off; off += D * 4;
-    s.all = off; off = (int)align_up((size_t)off + (xd ? G * S * 4 : 0), 16);   // the group's G lists
-    s.own = off; off = (int)align_up((size_t)off + (xd ? NWARP * G * D * 4 : 0), 16);  // partial sums
-    s.recv = off; off = (int)align_up((size_t)off + (xd ? G * D * 4 : 0), 16);  // partial sums received
+    // group dedup: the group's G lists, then (after them) the partial sums of the NWARP warps,
+    // over the points and chunk arrays when these are large enough (the lists are pushed
+    // only once every CTA of the group is past F); the partial sums received, their own
+    const int xall = xd ? max(G * S * 4, NWARP * G * D * 4) : 0;
+    if (s.hot - s.t >= xall) {
+        s.all = s.t;
+    } else {
+        s.all = off;
+        off = (int)align_up((size_t)off + xall, 16);
+    }
+    s.own = s.all;
+    s.recv = off; off = (int)align_up((size_t)off + (xd ? G * D * 4 : 0), 16);
     s.misc = off; off += 32 * 4;
     s.total = (int)align_up((size_t)off, 128);
     return s;
@@ -476,7 +495,9 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
             int *all = reinterpret_cast<int *>(smem + lay.all);      // [G][S]: every head's list
             float *red = reinterpret_cast<float *>(smem + lay.own);  // [NW][G][D] partial sums
             float *recv = reinterpret_cast<float *>(smem + lay.recv);  // [G][D]
-            // push this head's sorted list into slot `me` of every CTA of the group
+            // push this head's sorted list into slot `me` of every CTA of the group, once
+            // every CTA is past F (the lists overlay its points and chunk arrays)
+            cl.sync();
 #pragma unroll
             for (int k = 0; k < G; ++k) {
                 int *dst = cl.map_shared_rank(all, k) + me * S;
@@ -545,7 +566,9 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
                         }
                 }
             }
-            // partial sums of this CTA for each head -> slot `me` of that head's CTA
+            // partial sums of this CTA for each head (over the lists: once every warp is past
+            // them) -> slot `me` of that head's CTA
+            team_sync<BAR, NTH>();
 #pragma unroll
             for (int k = 0; k < G; ++k)
 #pragma unroll

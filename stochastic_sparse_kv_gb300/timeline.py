@@ -27,8 +27,8 @@ COLS = 16
 
 # two-pass layout: the score kernel's stamps (columns) and the value stage's phases
 SCORE_MARKS = {"producer done": 1, "roles done": 2, "cta end": 3}
-VALUE_PHASES = (("A chunk data", 1, 2), ("B fixed point + hot", 2, 3), ("C heavy keys", 3, 4),
-                ("D re-score", 4, 5), ("E prefix", 5, 6), ("F search", 6, 7), ("F discards", 7, 8),
+VALUE_PHASES = (("A chunk data", 1, 2), ("B fixed point, hot, heavy", 2, 3),
+                ("D re-score", 3, 5), ("E prefix", 5, 6), ("F search", 6, 7), ("F discards", 7, 8),
                 ("G index out + loads", 8, 9), ("G reduce + out", 9, 10))
 # single-pass cluster kernel: absolute marks and the phases between consecutive stamps
 CLUSTER_MARKS = {"setup done": 1, "producer done": 2, "score roles done": 3, "value stage start": 5,
@@ -94,8 +94,10 @@ def _median_over_calls(results: list) -> dict:
 
 
 def run(w: workloads.Workload, S: int, mode: str = "systematic", two_pass: bool = False, bernoulli: bool = False,
-        group_dedup: bool = False, calls: int = 20, warmup: int = 5, device: str = "cuda:0") -> dict:
-    lib = santa.load(_build.build(timeline=True))
+        group_dedup: bool = False, calls: int = 20, warmup: int = 5, device: str = "cuda:0",
+        library: str | None = None) -> dict:
+    """`library`: a stamped build to load instead of building libsanta_timeline.so."""
+    lib = santa.load(library or _build.build(timeline=True))
     dev = torch.device(device)
     torch.cuda.set_device(dev)
     q, k, v, sl = workloads.make_inputs_device(w, dev)
@@ -134,7 +136,8 @@ def run(w: workloads.Workload, S: int, mode: str = "systematic", two_pass: bool 
 
 def report(r: dict) -> str:
     f = lambda x: "   -  " if x is None else f"{x:6.2f}"  # noqa: E731
-    lines = [f"== {r['workload']} S={r['S']} {r['mode']} ({r['layout']}, {r['launches']} launches): "
+    flags = "".join(f", {k.replace('_', ' ')}" for k in ("group_dedup", "bernoulli") if r.get(k))
+    lines = [f"== {r['workload']} S={r['S']} {r['mode']}{flags} ({r['layout']}, {r['launches']} launches): "
              f"event {r['event_us']:.1f} us (stamped build), end of last CTA {r['end']:.1f} us, CTAs {r['ctas']:.0f}"]
     for k, m in r["marks"].items():
         lines.append(f"  {k:28s} min {f(m['min'])} med {f(m['med'])} max {f(m['max'])}")
@@ -171,8 +174,10 @@ def main(argv=None):
     ap.add_argument("--calls", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--json", action="store_true")
+    ap.add_argument("--library", default=None, help="a stamped build (-DSANTA_TIMELINE) to load instead")
     a = ap.parse_args(argv)
-    r = run(_workload(a.workload), a.S, a.mode, a.two_pass, a.bernoulli, a.group_dedup, a.calls, a.warmup)
+    r = run(_workload(a.workload), a.S, a.mode, a.two_pass, a.bernoulli, a.group_dedup, a.calls, a.warmup,
+            library=a.library)
     print(json.dumps(r) if a.json else report(r))
 
 
