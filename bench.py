@@ -353,7 +353,7 @@ def run_ours(args):
         gdd[str(S2)] = row
 
     # every configuration of the workload table, each mode (inputs drawn on the device)
-    wl = {}
+    wl, gdd_w = {}, {}
     if not args.no_extras and not args.no_workloads:
         for w2, S_list in workload_table(workloads):
             log(f"[bench] workload {w2.name} ...")
@@ -387,6 +387,25 @@ def run_ours(args):
                                "launches": santa.call_info(santa.make_shape(w2.B, w2.H_q, w2.H_kv, w2.d, w2.n_max),
                                                            S2, m)}
                     del plans2
+            if w2.heavy_frac > 0:
+                # the heavy-hitter batch is where the heads of a group share sampled rows: the
+                # opt-in group deduplication against the default, as for the headline batch
+                row_all = {}
+                for S2 in (256, 2048):
+                    row = {}
+                    for flag in (False, True):
+                        pl = santa.DecodePlan(q2, k2, v2, sl2, S2, "systematic", out=o2, want_idx=False,
+                                              stream=stream, group_dedup=flag)
+                        sb = [0]
+
+                        def f(pl=pl, sb=sb):
+                            sb[0] += 1
+                            pl(sb[0])
+                        tm, _ = time_steps(f, extra_steps, 3, stream, dist)
+                        row["group_dedup" if flag else "per_head"] = round(tm * 1000 / extra_steps, 2)
+                        del pl
+                    row_all[str(S2)] = row
+                gdd_w[w2.name] = row_all
             del q2, k2, v2, sl2, o2, caches
             torch.cuda.empty_cache()
         for key in list(wl):
@@ -458,7 +477,7 @@ def run_ours(args):
             "S_sweep_stratified": sweep_strat,
             "variants_us_per_step": variants,
             "workloads": wl,
-            "group_dedup_us_per_step": gdd,
+            "group_dedup_us_per_step": {args.workload: gdd, **gdd_w},
             "multi_layer": ml,
         }
         print(json.dumps(rec), flush=True)
@@ -471,13 +490,14 @@ def workload_table(workloads):
     table = [(workloads.LLAMA_B1, (256,))]
     table += [(lw, (128, 256)) for lw in workloads.LONG]
     table.append((workloads.RAGGED, (256,)))
+    table.append((workloads.LONG_GLOBAL, (256,)))
     return table
 
 
 def pick_workload(name):
     from stochastic_sparse_kv_gb300 import workloads
     table = {workloads.BATCHED.name: workloads.BATCHED, workloads.LLAMA_B1.name: workloads.LLAMA_B1,
-             workloads.RAGGED.name: workloads.RAGGED}
+             workloads.RAGGED.name: workloads.RAGGED, workloads.LONG_GLOBAL.name: workloads.LONG_GLOBAL}
     for lw in workloads.LONG:
         table[lw.name] = lw
     if name not in table:

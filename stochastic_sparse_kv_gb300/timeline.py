@@ -157,7 +157,8 @@ def report(r: dict) -> str:
 
 
 def _workload(name: str) -> workloads.Workload:
-    table = {x.name: x for x in (workloads.LLAMA_B1, workloads.BATCHED, workloads.RAGGED, *workloads.LONG)}
+    table = {x.name: x for x in (workloads.LLAMA_B1, workloads.BATCHED, workloads.RAGGED, *workloads.LONG,
+                                 workloads.LONG_GLOBAL)}
     if name not in table:
         raise SystemExit(f"unknown workload {name}; one of {sorted(table)}")
     return table[name]

@@ -225,6 +225,30 @@ def test_bad_seq_len_sets_device_error_word():
 
 # ------------------------------------------------------------------ full-size workloads
 
+@pytest.mark.slow
+@pytest.mark.parametrize("score_std", [0.05, 0.5])
+@pytest.mark.parametrize("mode", ["systematic", "stratified"])
+def test_near_flat_scores_at_32k_and_beyond(score_std, mode):
+    """Near-flat scores over long sequences: nearly every chunk lies within tau of the
+    maximum, far more than the HCAP chunks that can be re-scored, so the histogram keeps
+    the hottest and the rest stay as the tensor cores scored them.  32768 and 40000 keys."""
+    seq = [32768, 40000]
+    w, q, k, v, sl = workloads.small("flat_long", 2, 8, 2, 128, 40000, 512, seq_lens=seq,
+                                     score_std=score_std, seed=int(score_std * 100) + 11)
+    out, idx = run(q, k, v, sl, 512, mode, seed=6)
+    o_ref, i_ref = oracle.decode(q, k, v, sl, 512, mode, seed=6)
+    nm, npts = check_indices(idx, i_ref, q, k, sl, 512, mode, 6)
+    check_estimator(out.numpy(), idx, v, sl, o_ref)
+    print(f"\n[near-flat] std {score_std} {mode}: {nm} boundary mismatches of {npts} points")
+
+
+@pytest.mark.slow
+def test_llama_b1_200k_chunk_arrays_in_global_memory():
+    """Beyond 131072 keys the value stage searches chunk arrays in global memory: every
+    head of a Llama-shaped 200k-key sequence against the oracle, in every mode."""
+    print(_full_check(workloads.LONG_GLOBAL, ("systematic", "stratified", "iid", "dense")))
+
+
 def _sampled_pairs(B, H_q, n, seed):
     rs = np.random.default_rng(seed)
     return [(int(b), int(h)) for b, h in zip(rs.integers(0, B, n), rs.integers(0, H_q, n))]
