@@ -27,8 +27,8 @@ COLS = 16
 
 # two-pass layout: the score kernel's stamps (columns) and the value stage's phases
 SCORE_MARKS = {"producer done": 1, "roles done": 2, "cta end": 3}
-VALUE_PHASES = (("A chunk data", 1, 2), ("B fixed point, hot, heavy", 2, 3),
-                ("D re-score", 3, 5), ("E prefix", 5, 6), ("F search", 6, 7), ("F discards", 7, 8),
+VALUE_PHASES = (("A chunk data", 1, 2), ("B fixed point + hot", 2, 3), ("C heavy keys", 3, 4),
+                ("D re-score", 4, 5), ("E prefix", 5, 6), ("F search", 6, 7), ("F discards", 7, 8),
                 ("G index out + loads", 8, 9), ("G reduce + out", 9, 10))
 # single-pass cluster kernel: absolute marks and the phases between consecutive stamps
 CLUSTER_MARKS = {"setup done": 1, "producer done": 2, "score roles done": 3, "value stage start": 5,
