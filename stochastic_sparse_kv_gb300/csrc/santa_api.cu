@@ -536,8 +536,9 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     const void *fn2 = nullptr;
     int smem2 = 0;
     if (!dense) {
-        fn2 = (D == 128) ? kernel_d128(KIND_GATHER, G) : kernel_d64(KIND_GATHER, G);
         p.xdedup = ((mode_flags & SANTA_GROUP_DEDUP) && gather_xdedup(G, p.S)) ? 1 : 0;
+        const int kind2 = KIND_GATHER + (p.xdedup ? GATHER_XD : 0) + (mode == MODE_IID ? GATHER_IID : 0);
+        fn2 = (D == 128) ? kernel_d128(kind2, G) : kernel_d64(kind2, G);
         smem2 = gather_smem_bytes(D, G, p.S, p.nch, mode, p.xdedup != 0);
         if (smem2 > optin) return SANTA_ERR_UNSUPPORTED;
         int occ2 = 0;

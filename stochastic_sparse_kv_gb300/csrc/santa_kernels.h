@@ -4,7 +4,8 @@
 
 namespace santa {
 
-enum KernelKind : int { KIND_SCORE = 0, KIND_DENSE = 1, KIND_GATHER = 2, KIND_DMERGE = 3, KIND_CLUSTER = 4 };
+// KIND_GATHER + v: the value-stage kernel of variant v (GATHER_XD | GATHER_IID bits)
+enum KernelKind : int { KIND_SCORE = 0, KIND_DENSE = 1, KIND_DMERGE = 3, KIND_CLUSTER = 4, KIND_GATHER = 8 };
 
 // Kernel entry for (kind, G) at head dimension 64 or 128, or nullptr.
 const void *kernel_d64(int kind, int G);

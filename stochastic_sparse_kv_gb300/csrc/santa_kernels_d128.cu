@@ -9,12 +9,23 @@ namespace santa {
 
 const void *kernel_d128(int kind, int G)
 {
-    if (kind == KIND_GATHER) {
-        switch (G) {
-        case 1: return (const void *)santa_gather_kernel<128, 1>;
-        case 2: return (const void *)santa_gather_kernel<128, 2>;
-        case 4: return (const void *)santa_gather_kernel<128, 4>;
-        case 8: return (const void *)santa_gather_kernel<128, 8>;
+    if (kind >= KIND_GATHER && kind < KIND_GATHER + 4) {  // (group dedup needs G > 1)
+        const int v = kind - KIND_GATHER;
+        switch (G * 4 + v) {
+        case 4: return (const void *)santa_gather_kernel<128, 1, 0>;
+        case 6: return (const void *)santa_gather_kernel<128, 1, GATHER_IID>;
+        case 8: return (const void *)santa_gather_kernel<128, 2, 0>;
+        case 9: return (const void *)santa_gather_kernel<128, 2, GATHER_XD>;
+        case 10: return (const void *)santa_gather_kernel<128, 2, GATHER_IID>;
+        case 11: return (const void *)santa_gather_kernel<128, 2, GATHER_XD | GATHER_IID>;
+        case 16: return (const void *)santa_gather_kernel<128, 4, 0>;
+        case 17: return (const void *)santa_gather_kernel<128, 4, GATHER_XD>;
+        case 18: return (const void *)santa_gather_kernel<128, 4, GATHER_IID>;
+        case 19: return (const void *)santa_gather_kernel<128, 4, GATHER_XD | GATHER_IID>;
+        case 32: return (const void *)santa_gather_kernel<128, 8, 0>;
+        case 33: return (const void *)santa_gather_kernel<128, 8, GATHER_XD>;
+        case 34: return (const void *)santa_gather_kernel<128, 8, GATHER_IID>;
+        case 35: return (const void *)santa_gather_kernel<128, 8, GATHER_XD | GATHER_IID>;
         }
         return nullptr;
     }
