@@ -21,9 +21,9 @@ int score_smem_bytes(int D, int G, int B)
     return score_smem(D, B).total;
 }
 
-int gather_smem_bytes(int D, int G, int S, int nch_used, int mode, bool xdedup)
+int gather_smem_bytes(int D, int G, int S, int nch_used, int mode, bool xdedup, int nth)
 {
-    return gather_smem(D, G, S, nch_used, mode, xdedup).total;
+    return gather_smem(D, G, S, nch_used, mode, xdedup, nth).total;
 }
 
 int dense_smem_bytes(int D, int G, int B)
@@ -534,15 +534,24 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
     int occ = 0;
     if ((rc = prepare_fn(fn, dev, smem, threads, &occ))) return rc;
     const void *fn2 = nullptr;
-    int smem2 = 0;
+    int smem2 = 0, nth2 = NT;
     if (!dense) {
         p.xdedup = ((mode_flags & SANTA_GROUP_DEDUP) && gather_xdedup(G, p.S)) ? 1 : 0;
-        const int kind2 = KIND_GATHER + (p.xdedup ? GATHER_XD : 0) + (mode == MODE_IID ? GATHER_IID : 0);
+        // at most one head per SM and long sequences: the wide team (four times the threads
+        // on each phase's loops over chunks, and the chunk arrays in shared memory up to
+        // 2.5 times as many chunks; measured slower than the narrow team at 1024 chunks,
+        // faster at 4096)
+        nth2 = NT;
+        if (!p.xdedup && (long long)shape->B * shape->H_q <= sms && p.nch > NCH_WIDE_MIN &&
+            gather_smem_bytes(D, G, p.S, p.nch, mode, false, NT_WIDE) <= optin)
+            nth2 = NT_WIDE;
+        const int kind2 = KIND_GATHER + (p.xdedup ? GATHER_XD : 0) + (mode == MODE_IID ? GATHER_IID : 0) +
+                          (nth2 == NT_WIDE ? GATHER_WIDE : 0);
         fn2 = (D == 128) ? kernel_d128(kind2, G) : kernel_d64(kind2, G);
-        smem2 = gather_smem_bytes(D, G, p.S, p.nch, mode, p.xdedup != 0);
+        smem2 = gather_smem_bytes(D, G, p.S, p.nch, mode, p.xdedup != 0, nth2);
         if (smem2 > optin) return SANTA_ERR_UNSUPPORTED;
         int occ2 = 0;
-        if ((rc = prepare_fn(fn2, dev, smem2, NT, &occ2))) return rc;
+        if ((rc = prepare_fn(fn2, dev, smem2, nth2, &occ2))) return rc;
     }
     const long long items = (long long)shape->B * shape->H_kv * ((shape->n_max + L - 1) / L);
     long long grid = (long long)sms * occ;
@@ -600,7 +609,7 @@ int santa_decode(const santa_shape *shape, const void *q, const void *k_cache, c
         // the G heads of a group form a cluster when they share V loads
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3((unsigned)(shape->B * shape->H_q));
-        cfg.blockDim = dim3(NT);
+        cfg.blockDim = dim3((unsigned)nth2);
         cfg.dynamicSmemBytes = (size_t)smem2;
         cfg.stream = (cudaStream_t)stream;
         cudaLaunchAttribute attr[2];

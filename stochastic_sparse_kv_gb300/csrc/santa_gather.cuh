@@ -35,16 +35,25 @@
 namespace santa {
 
 constexpr int NCH_SMEM = 4096;  // a head's chunk arrays stay in shared memory up to this many chunks
+constexpr int NT_WIDE = 1024;   // the team of the wide variant (one CTA per SM: small batches)
+constexpr int NCH_SMEM_WIDE = 10240;  // its chunk arrays stay in shared memory up to this many chunks
+constexpr int NCH_WIDE_MIN = 2048;    // the wide variant for sequences of more chunks than this
+__host__ __device__ constexpr int nch_smem_cap(int nth) { return nth > NT ? NCH_SMEM_WIDE : NCH_SMEM; }
 constexpr int HCAP = 192;       // hot chunks re-scored per head, at most
 constexpr int HBINS = 256;      // histogram bins that pick the hottest HCAP chunks
 constexpr int XDEDUP_MAX = 8192;  // G * S up to which the group's heads share their V loads
-enum : int { GATHER_XD = 1, GATHER_IID = 2 };  // value-stage kernel variants (bits)
+// value-stage kernel variants (bits): group dedup, i.i.d. points, and the wide team of
+// NT_WIDE threads for batches of at most one head per SM (not with group dedup)
+enum : int { GATHER_XD = 1, GATHER_IID = 2, GATHER_WIDE = 4 };
 
 // Whether the value stage can run as clusters of the group's G heads that load each
 // distinct V row once for all of them (on request: SANTA_GROUP_DEDUP; the host then
 // launches clusters of G and sets Params::xdedup).
 __host__ __device__ inline bool gather_xdedup(int G, int S) { return G > 1 && G * S <= XDEDUP_MAX; }
 constexpr int HKCAP = 512;      // heavy keys re-scored per head, at most
+
+// misc words of the value stage (GM_SCAN: the block scan's NTH/32 + 1 64-bit words)
+enum : int { GM_MAX = 0, GM_CMAX = 1, GM_NHOT = 2, GM_NHV = 3, GM_CNT = 4, GM_SCAN = 8 };
 
 struct GatherSmem {
     int t, O, tot, ce, cm, hot, hv, hvw, hist, idx, lead, acc, qf, all, own, recv, misc, total;
@@ -56,7 +65,7 @@ __host__ __device__ inline GatherSmem gather_smem(int D, int G, int S, int nch_u
 {
     GatherSmem s{};
     const int Sp = (mode == MODE_IID) ? next_pow2(S) : S;
-    const int ncs = nch_used <= NCH_SMEM ? nch_used : 0;
+    const int ncs = nch_used <= nch_smem_cap(nth) ? nch_used : 0;
     int off = 0;
     s.t = off; off += S * 8;
     s.O = off; off += ncs * 8;
@@ -93,12 +102,11 @@ __host__ __device__ inline GatherSmem gather_smem(int D, int G, int S, int nch_u
     }
     s.own = s.all;
     s.recv = off; off = (int)align_up((size_t)off + (xd ? G * D * 4 : 0), 16);
-    s.misc = off; off += 32 * 4;
+    s.misc = off; off += (int)align_up((size_t)max(32, GM_SCAN + 2 * (nth / 32 + 1)) * 4, 16);
     s.total = (int)align_up((size_t)off, 128);
     return s;
 }
 
-enum : int { GM_MAX = 0, GM_CMAX = 1, GM_NHOT = 2, GM_NHV = 3, GM_CNT = 4, GM_SCAN = 8 /* NWARP+1 words */ };
 
 // Barrier of a team of NTH threads: the whole CTA (BAR = 0) or named barrier BAR.
 template <int BAR, int NTH>
@@ -227,7 +235,7 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
     const int b = bh / H_q, h = bh % H_q, g = h / G;
     (void)h;
     const int nchn = (n + CHUNK - 1) / CHUNK;  // chunks of this sequence
-    const bool in_smem = p.nch <= NCH_SMEM;
+    const bool in_smem = p.nch <= nch_smem_cap(NTH);
     const size_t bhc = (size_t)bh * p.nch;
     uint64_t *tfx = reinterpret_cast<uint64_t *>(smem + lay.t);
     // the head's chunk arrays: shared-memory copies, or the workspace itself
@@ -659,24 +667,25 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
 // points) select the paths at compile time, so that each launch carries only the code it
 // runs (the value stage runs each phase once per CTA: fetching a larger kernel's
 // instructions measured about 4 us slower at B=16).
-template <int D, int G, int VAR>
-__global__ void __launch_bounds__(NT, 4) santa_gather_kernel(const Params p)
+template <int D, int G, int VAR, int NTH = (VAR & GATHER_WIDE) ? NT_WIDE : NT>
+__global__ void __launch_bounds__(NTH, NTH == NT ? 4 : 1) santa_gather_kernel(const Params p)
 {
     constexpr bool XD = (VAR & GATHER_XD) != 0 && G > 1, IID = (VAR & GATHER_IID) != 0;
+    static_assert(!(XD && NTH != NT), "group dedup runs with the narrow team");
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, bh = blockIdx.x;
     if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 0);
     const int n = value_len(p, bh / p.H_q);
     if (n == 0) {  // (every CTA of a cluster shares b, so all of them leave here)
-        value_empty<D, NT>(p, bh, tid);
+        value_empty<D, NTH>(p, bh, tid);
         return;
     }
-    const GatherSmem lay = gather_smem(D, G, p.S, p.nch, p.mode, XD);
-    value_prologue<D, G, NT, 0, IID>(p, bh, smem, lay, tid);
+    const GatherSmem lay = gather_smem(D, G, p.S, p.nch, p.mode, XD, NTH);
+    value_prologue<D, G, NTH, 0, IID>(p, bh, smem, lay, tid);
     pdl_wait();  // the score kernel's results are complete and visible from here on
     __syncthreads();
     if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 1);
-    value_main<D, G, NT, 0, XD>(p, bh, n, smem, lay, tid);
+    value_main<D, G, NTH, 0, XD>(p, bh, n, smem, lay, tid);
 }
 
 }  // namespace santa

@@ -9,23 +9,31 @@ namespace santa {
 
 const void *kernel_d128(int kind, int G)
 {
-    if (kind >= KIND_GATHER && kind < KIND_GATHER + 4) {  // (group dedup needs G > 1)
+    if (kind >= KIND_GATHER && kind < KIND_GATHER + 8) {  // (group dedup: G > 1, narrow team)
         const int v = kind - KIND_GATHER;
-        switch (G * 4 + v) {
-        case 4: return (const void *)santa_gather_kernel<128, 1, 0>;
-        case 6: return (const void *)santa_gather_kernel<128, 1, GATHER_IID>;
-        case 8: return (const void *)santa_gather_kernel<128, 2, 0>;
-        case 9: return (const void *)santa_gather_kernel<128, 2, GATHER_XD>;
-        case 10: return (const void *)santa_gather_kernel<128, 2, GATHER_IID>;
-        case 11: return (const void *)santa_gather_kernel<128, 2, GATHER_XD | GATHER_IID>;
-        case 16: return (const void *)santa_gather_kernel<128, 4, 0>;
-        case 17: return (const void *)santa_gather_kernel<128, 4, GATHER_XD>;
-        case 18: return (const void *)santa_gather_kernel<128, 4, GATHER_IID>;
-        case 19: return (const void *)santa_gather_kernel<128, 4, GATHER_XD | GATHER_IID>;
-        case 32: return (const void *)santa_gather_kernel<128, 8, 0>;
-        case 33: return (const void *)santa_gather_kernel<128, 8, GATHER_XD>;
-        case 34: return (const void *)santa_gather_kernel<128, 8, GATHER_IID>;
-        case 35: return (const void *)santa_gather_kernel<128, 8, GATHER_XD | GATHER_IID>;
+        switch (G * 8 + v) {
+        case 8: return (const void *)santa_gather_kernel<128, 1, 0>;
+        case 10: return (const void *)santa_gather_kernel<128, 1, GATHER_IID>;
+        case 12: return (const void *)santa_gather_kernel<128, 1, GATHER_WIDE>;
+        case 14: return (const void *)santa_gather_kernel<128, 1, GATHER_IID | GATHER_WIDE>;
+        case 16: return (const void *)santa_gather_kernel<128, 2, 0>;
+        case 17: return (const void *)santa_gather_kernel<128, 2, GATHER_XD>;
+        case 18: return (const void *)santa_gather_kernel<128, 2, GATHER_IID>;
+        case 19: return (const void *)santa_gather_kernel<128, 2, GATHER_XD | GATHER_IID>;
+        case 20: return (const void *)santa_gather_kernel<128, 2, GATHER_WIDE>;
+        case 22: return (const void *)santa_gather_kernel<128, 2, GATHER_IID | GATHER_WIDE>;
+        case 32: return (const void *)santa_gather_kernel<128, 4, 0>;
+        case 33: return (const void *)santa_gather_kernel<128, 4, GATHER_XD>;
+        case 34: return (const void *)santa_gather_kernel<128, 4, GATHER_IID>;
+        case 35: return (const void *)santa_gather_kernel<128, 4, GATHER_XD | GATHER_IID>;
+        case 36: return (const void *)santa_gather_kernel<128, 4, GATHER_WIDE>;
+        case 38: return (const void *)santa_gather_kernel<128, 4, GATHER_IID | GATHER_WIDE>;
+        case 64: return (const void *)santa_gather_kernel<128, 8, 0>;
+        case 65: return (const void *)santa_gather_kernel<128, 8, GATHER_XD>;
+        case 66: return (const void *)santa_gather_kernel<128, 8, GATHER_IID>;
+        case 67: return (const void *)santa_gather_kernel<128, 8, GATHER_XD | GATHER_IID>;
+        case 68: return (const void *)santa_gather_kernel<128, 8, GATHER_WIDE>;
+        case 70: return (const void *)santa_gather_kernel<128, 8, GATHER_IID | GATHER_WIDE>;
         }
         return nullptr;
     }

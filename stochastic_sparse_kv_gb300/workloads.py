@@ -61,9 +61,11 @@ RAGGED = Workload("llama8b_ragged_b32", 32, 32, 8, 128, 65536, 256, ("systematic
 LONG = tuple(Workload(f"llama8b_b4_{n // 1024}k", 4, 32, 8, 128, n, 256,
                       ("systematic", "stratified", "dense")) for n in (8192, 32768, 131072))
 BATCHED_S_SWEEP = (64, 128, 256, 512)
-# Beyond 131072 keys (4096 chunks of 32) the value stage keeps a head's chunk arrays in
-# global memory instead of shared memory: one sequence of that length, Llama-shaped.
-LONG_GLOBAL = Workload("llama8b_b1_200k", 1, 32, 8, 128, 200000, 256, ("systematic", "stratified", "dense"))
+# A value-stage CTA keeps a head's chunk arrays in shared memory up to 4096 chunks of 32
+# keys (131072 keys), or 10240 chunks (327680 keys) when the batch has at most one head
+# per SM (its wide team of 1024 threads); beyond that they stay in global memory.  One
+# Llama-shaped sequence of 400000 keys takes that path.
+LONG_GLOBAL = Workload("llama8b_b1_400k", 1, 32, 8, 128, 400000, 256, ("systematic", "stratified", "dense"))
 
 
 def seq_lens_for(w: Workload) -> torch.Tensor:

@@ -57,7 +57,9 @@ CASES = [
     (64, 8, 4, 2500, [2500, 2048], 128),
     (64, 16, 4, 900, [900, 64, 129], 256),
     (64, 64, 8, 700, [700, 311], 48),
-    # more than 4096 chunks: the value stage keeps its chunk arrays in global memory
+    # more than 4096 chunks: in shared memory only for the wide value stage (one head per
+    # SM and more than 2048 chunks, as here; test_chunk_arrays_in_global_memory_narrow_team
+    # covers the narrow one)
     (64, 8, 2, 140000, [140000, 3000], 200),
     # G * S above the cluster limit: each head gathers its own rows
     (128, 32, 8, 1500, [1500, 800], 4096),
@@ -243,10 +245,23 @@ def test_near_flat_scores_at_32k_and_beyond(score_std, mode):
 
 
 @pytest.mark.slow
-def test_llama_b1_200k_chunk_arrays_in_global_memory():
-    """Beyond 131072 keys the value stage searches chunk arrays in global memory: every
-    head of a Llama-shaped 200k-key sequence against the oracle, in every mode."""
+def test_llama_b1_400k_chunk_arrays_in_global_memory():
+    """Beyond 10240 chunks the wide value stage (one head per SM) searches chunk arrays in
+    global memory: every head of a Llama-shaped 400k-key sequence against the oracle, in
+    every mode."""
     print(_full_check(workloads.LONG_GLOBAL, ("systematic", "stratified", "iid", "dense")))
+
+
+@pytest.mark.parametrize("mode", ["systematic", "iid"])
+def test_chunk_arrays_in_global_memory_narrow_team(mode):
+    """More heads than SMs (the 256-thread value stage) and more than 4096 chunks: the
+    chunk arrays stay in global memory."""
+    seq = [140000, 2000]
+    w, q, k, v, sl = workloads.small("narrow_global", 2, 80, 10, 64, 140000, 128, seq_lens=seq, seed=29)
+    out, idx = run(q, k, v, sl, 128, mode, seed=3)
+    o_ref, i_ref = oracle.decode(q, k, v, sl, 128, mode, seed=3)
+    check_indices(idx, i_ref, q, k, sl, 128, mode, 3)
+    check_estimator(out.numpy(), idx, v, sl, o_ref)
 
 
 def _sampled_pairs(B, H_q, n, seed):
