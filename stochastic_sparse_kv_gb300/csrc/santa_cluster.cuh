@@ -611,22 +611,16 @@ __global__ void __launch_bounds__(CL_NT, 1)
                 const int j0 = c * CHUNK;
                 const int jn = min(CHUNK, nkl - j0);
                 const float4 *w4p = reinterpret_cast<const float4 *>(w_s + h * LW + j0);
-                float P = 0.f;
-                int pick = -1, lastpos = 0;
+                float wv[CHUNK];
 #pragma unroll
                 for (int k4 = 0; k4 < CHUNK / 4; ++k4) {
                     const float4 xv = w4p[k4];
-                    const float xs[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k = 4 * k4 + e;
-                        const float xw = k < jn ? xs[e] : 0.f;
-                        P = __fadd_rn(P, xw);
-                        if (xw > 0.f) lastpos = k;
-                        if (pick < 0 && P > rres) pick = k;
-                    }
+                    wv[4 * k4] = xv.x;
+                    wv[4 * k4 + 1] = xv.y;
+                    wv[4 * k4 + 2] = xv.z;
+                    wv[4 * k4 + 3] = xv.w;
                 }
-                if (pick < 0) pick = lastpos;
+                const int pick = chunk_pick(wv, jn, rres);
                 j = key0 + j0 + pick;
                 if (p.idx_out) p.idx_out[((size_t)grp * G + h) * S + s] = j;
                 const uint16_t *vrow = p.v + ((size_t)grp * p.n_max + j) * D;  // gathered below

@@ -459,17 +459,8 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
             wv[4 * k4 + 2] = x.z;
             wv[4 * k4 + 3] = x.w;
         }
-        float P = 0.f;
-        int pick = -1, lastpos = 0;
-#pragma unroll
-        for (int k = 0; k < CHUNK; ++k) {
-            const float x = k < jn ? wv[k] : 0.f;
-            P = __fadd_rn(P, x);
-            if (x > 0.f) lastpos = k;
-            if (pick < 0 && P > rres) pick = k;
-        }
-        if (pick < 0) pick = lastpos;  // only when rounding put t past the chunk's mass
-        idx[s] = j0 + pick;            // (iid: overwrites this point's own uniform)
+        const int pick = chunk_pick(wv, jn, rres);
+        idx[s] = j0 + pick;  // (iid: overwrites this point's own uniform)
         // the V row this point selects: into L2 now, gathered in G
         const uint16_t *vrow = p.v + (((size_t)b * p.H_kv + g) * (size_t)p.n_max + (size_t)(j0 + pick)) * D;
         prefetch_l2(vrow);

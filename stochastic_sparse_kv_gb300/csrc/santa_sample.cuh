@@ -96,6 +96,28 @@ __device__ __forceinline__ void rescore_key_quad(const uint16_t *krow, const flo
 
 // ------------------------------------------------------------------ search helpers
 
+// The key of a chunk that a target selects: the first k whose running sum of the chunk's
+// weights (fp32, added in key order) exceeds the target's remainder r inside the chunk.
+// The running sum never decreases, so that k is the number of running sums <= r -- two
+// instructions a key instead of a branch.  When there is none (rounding put the target
+// past the chunk's mass) it is the chunk's last key of positive weight.
+__device__ __forceinline__ int chunk_pick(const float (&wv)[CHUNK], int jn, float r)
+{
+    float P = 0.f;
+    int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < CHUNK; ++k) {
+        P = __fadd_rn(P, k < jn ? wv[k] : 0.f);
+        cnt += (P <= r) ? 1 : 0;
+    }
+    if (cnt < CHUNK) return cnt;
+    int last = 0;
+#pragma unroll
+    for (int k = 0; k < CHUNK; ++k)
+        if (k < jn && wv[k] > 0.f) last = k;
+    return last;
+}
+
 __device__ __forceinline__ int lower_bound_i(const int *a, int n, int key)
 {
     int lo = 0, hi = n;
