@@ -461,10 +461,14 @@ __device__ __forceinline__ void value_main(const Params &p, int bh, int n, uint8
         }
         const int pick = chunk_pick(wv, jn, rres);
         idx[s] = j0 + pick;  // (iid: overwrites this point's own uniform)
-        // the V row this point selects: into L2 now, gathered in G
-        const uint16_t *vrow = p.v + (((size_t)b * p.H_kv + g) * (size_t)p.n_max + (size_t)(j0 + pick)) * D;
-        prefetch_l2(vrow);
-        if (D * 2 > 128) prefetch_l2(vrow + 64);
+        // the V row this point selects: into L2 now, gathered in G (with one point per
+        // thread; with several, the early V rows competed with the weights still to be
+        // read, and the search measured slower by more than the gather gained)
+        if (S <= NTH) {
+            const uint16_t *vrow = p.v + (((size_t)b * p.H_kv + g) * (size_t)p.n_max + (size_t)(j0 + pick)) * D;
+            prefetch_l2(vrow);
+            if (D * 2 > 128) prefetch_l2(vrow + 64);
+        }
     }
     team_sync<BAR, NTH>();
     if (tid == 0) SANTA_STAMP(TL_VALUE_ROW0 + bh, 7);
