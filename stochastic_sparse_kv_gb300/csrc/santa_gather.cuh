@@ -3,8 +3,9 @@
 // "Stochastic Sparse Attention for Memory-Bound Inference" (abstract): sample S << n_k
 // indices from the post-softmax distribution and aggregate only those value rows,
 // scaled by 1/S.  One CTA per (batch row b, query head h), launched as a programmatic
-// dependent of the score kernel: its CTAs take SMs as the score kernel's CTAs leave them
-// and draw their points before the dependency wait.  The score kernel left, per 32-key
+// dependent of the score kernel: its CTAs start once every score CTA has finished (they
+// cannot share an SM with one) and draw their points before the dependency wait.  The
+// score kernel left, per 32-key
 // chunk, the fp32 weights w_j in the chunk's scale 2^-c_t, the chunk total, c_t and the
 // chunk's maximum score.  After the dependency wait the work is a few wide phases, each
 // at most one round trip to memory, in integer or fp32 arithmetic only (written for a team
@@ -20,12 +21,13 @@
 //      heaviest keys' fp32 dot-product rounding would otherwise shift every later CDF
 //      boundary;
 //   E. the exact exclusive prefix O_c of the G_c (block scan), Z = the total;
-//   F. one thread per point: T = t Z, i = min{ j : W_j > T } by chunk -> key, and the
-//      selected V row prefetched into L2; then the head's weights and chunk data, read
-//      for the last time, are discarded from L2 (never written back);
+//   F. one thread per point: T = t Z, i = min{ j : W_j > T } by chunk -> key, and (with
+//      at most one point per thread) the selected V row prefetched into L2; then the
+//      head's weights and chunk data, read for the last time, are discarded from L2
+//      (never written back);
 //   G. the distinct sampled rows (ordered compaction of the sorted list), each loaded
-//      once -- 16-byte pieces spread over all threads, all in flight -- and added times
-//      its count; out = sum / S (fp32, or rounded once to bf16).
+//      once -- 16-byte pieces spread over all threads, eight in flight per thread -- and
+//      added times its count; out = sum / S (fp32, or rounded once to bf16).
 #pragma once
 
 #include <cooperative_groups.h>
@@ -179,14 +181,16 @@ __device__ __forceinline__ void value_prologue(const Params &p, int bh, uint8_t 
     const int Sp = IID ? next_pow2(S) : S;
     if constexpr (IID) {
         unsigned *uk = reinterpret_cast<unsigned *>(idx);
-        for (int s = tid; s < Sp; s += NTH) {
-            unsigned u = 0xffffffffu;
-            if (s < S) {
-                uint64_t rnd[4];
-                philox_block(p.seed, (uint64_t)(s / 4), b, h, 3, rnd);
-                u = (unsigned)(rnd[s % 4] >> 32);
+        // one Philox block per four points, drawn once (thread j draws block j); the
+        // padding up to a power of two sorts last
+        for (int j = tid; 4 * j < Sp; j += NTH) {
+            uint64_t rnd[4] = {0, 0, 0, 0};
+            if (4 * j < S) philox_block(p.seed, (uint64_t)j, b, h, 3, rnd);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int s = 4 * j + e;
+                if (s < Sp) uk[s] = s < S ? (unsigned)(rnd[e] >> 32) : 0xffffffffu;
             }
-            uk[s] = u;
         }
         team_sync<BAR, NTH>();
         for (int kk = 2; kk <= Sp; kk <<= 1)
@@ -206,9 +210,33 @@ __device__ __forceinline__ void value_prologue(const Params &p, int bh, uint8_t 
             }
         for (int s = tid; s < S; s += NTH) tfx[s] = (uint64_t)uk[s] << 32;  // u = x 2^-32 exactly
     } else {
-        // the fp64 point as a 64-bit fraction (t < 1; the scaling by 2^64 is exact)
-        for (int s = tid; s < S; s += NTH)
-            tfx[s] = __double2ull_rz(__dmul_rn(sample_point(p.mode, p.seed, b, h, s, p.rS), 0x1p64));
+        // The Philox blocks, each drawn once: one per head (systematic: every point shares
+        // its uniform), or one per four points (stratified: the raw words wait in the point
+        // array until each thread replaces its own with its point).  Then the fp64 point
+        // as a 64-bit fraction (t < 1; the scaling by 2^64 is exact), as sample_point.
+        const bool sys = p.mode == MODE_SYSTEMATIC;
+        uint64_t *w0 = reinterpret_cast<uint64_t *>(misc + GM_SCAN);
+        if (sys) {
+            if (tid == 0) {
+                uint64_t rnd[4];
+                philox_block(p.seed, 0, b, h, 2, rnd);
+                *w0 = rnd[0];
+            }
+        } else {
+            for (int j = tid; 4 * j < S; j += NTH) {
+                uint64_t rnd[4];
+                philox_block(p.seed, (uint64_t)j, b, h, 1, rnd);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (4 * j + e < S) tfx[4 * j + e] = rnd[e];
+            }
+        }
+        team_sync<BAR, NTH>();
+        for (int s = tid; s < S; s += NTH) {
+            const double t = sys ? __dmul_rn(__dadd_rn(word_uniform(*w0), (double)s), p.rS)
+                                 : __dmul_rn(__dadd_rn((double)s, word_uniform(tfx[s])), p.rS);
+            tfx[s] = __double2ull_rz(__dmul_rn(t, 0x1p64));
+        }
     }
     for (int i = tid; i < D; i += NTH) qf[i] = __uint_as_float((uint32_t)p.q[(size_t)bh * D + i] << 16);
     if (tid == 0) {
