@@ -420,8 +420,42 @@ __global__ void __launch_bounds__(CL_NT, 1)
                 }
             for (int i = pt; i < G * S; i += NPT) tfx[i] = (uint64_t)sortk[(i / S) * Sp + i % S] << 32;
         } else {
-            for (int i = pt; i < G * S; i += NPT)
-                tfx[i] = __double2ull_rz(__dmul_rn(sample_point(p.mode, p.seed, b, g * G + i / S, i % S, p.rS), 0x1p64));
+            // each Philox block drawn once: one per head (systematic: the head's points share
+            // its uniform) or one per four points (stratified); the raw words wait in the
+            // point array until the points replace them, as sample_point computes them
+            const bool sys = p.mode == MODE_SYSTEMATIC;
+            if (sys) {
+                for (int h = pt; h < G; h += NPT) {
+                    uint64_t rnd[4];
+                    philox_block(p.seed, 0, b, g * G + h, 2, rnd);
+                    tfx[h * S] = rnd[0];
+                }
+            } else {
+                const int nb = (S + 3) / 4;
+                for (int k = pt; k < G * nb; k += NPT) {
+                    const int h = k / nb, jb = k % nb;
+                    uint64_t rnd[4];
+                    philox_block(p.seed, (uint64_t)jb, b, g * G + h, 1, rnd);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (4 * jb + e < S) tfx[h * S + 4 * jb + e] = rnd[e];
+                }
+            }
+            asm volatile("bar.sync %0, %1;" ::"n"(CL_PTS_BAR), "n"(NPT) : "memory");
+            uint64_t w0[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) w0[h] = sys ? tfx[h * S] : 0;
+            asm volatile("bar.sync %0, %1;" ::"n"(CL_PTS_BAR), "n"(NPT) : "memory");
+            for (int i = pt; i < G * S; i += NPT) {
+                const int h = i / S, si = i % S;
+                uint64_t wh = 0;
+#pragma unroll
+                for (int k = 0; k < G; ++k)
+                    if (k == h) wh = w0[k];
+                const double t = sys ? __dmul_rn(__dadd_rn(word_uniform(wh), (double)si), p.rS)
+                                     : __dmul_rn(__dadd_rn((double)si, word_uniform(tfx[i])), p.rS);
+                tfx[i] = __double2ull_rz(__dmul_rn(t, 0x1p64));
+            }
         }
     }
 
