@@ -38,10 +38,12 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "santa_decode_b16_32k_traffic.t
 CSRC = os.path.join("stochastic_sparse_kv_gb300", "csrc")
 KERNEL_SOURCES = [os.path.join(CSRC, f) for f in ("santa_common.cuh", "santa_sample.cuh", "santa_tcgen05.cuh", "santa_score.cuh",
                                                    "santa_gather.cuh", "santa_dense.cuh", "santa_cluster.cuh",
+                                                   "santa_kernels.h", "santa_kernels_d128.cu", "santa_kernels_d64.cu",
                                                    "santa_api.cu")]
 # The sampled path is two launches chained by programmatic dependent launch (the value
-# stage overlaps the score kernel's tail), so one santa_decode call is timed as the unit.
-ROOFLINE_UNIT = "santa_decode: santa_score_kernel<128,4> + santa_gather_kernel<128,4> (PDL-chained)"
+# stage's launch and prologue overlap the score grid's end), so one santa_decode call is
+# timed as the unit.
+ROOFLINE_UNIT = "santa_decode: santa_score_kernel<128,4> + santa_gather_kernel<128,4,0,256> (PDL-chained)"
 ROOFLINE_UNIT_DENSE = "santa_decode (dense): santa_dense_kernel<128,4> + santa_dense_merge_kernel<128> (PDL-chained)"
 
 

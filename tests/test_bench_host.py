@@ -39,3 +39,11 @@ def test_traffic_record_is_used_only_for_the_sources_it_was_taken_on():
         assert v == float(rec["traffic_bytes_per_launch"]) and v > 0
     else:
         assert v is None
+
+
+def test_traffic_record_key_covers_every_kernel_source():
+    # a change to any kernel source, dispatch table or host launch code invalidates it
+    import os
+    csrc = os.path.join(bench.ROOT, bench.CSRC)
+    files = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    assert sorted(os.path.basename(s) for s in bench.KERNEL_SOURCES) == files
