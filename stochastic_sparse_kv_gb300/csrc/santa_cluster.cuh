@@ -422,7 +422,8 @@ __global__ void __launch_bounds__(CL_NT, 1)
         } else {
             // each Philox block drawn once: one per head (systematic: the head's points share
             // its uniform) or one per four points (stratified); the raw words wait in the
-            // point array until the points replace them, as sample_point computes them
+            // point array until the points replace them (in integers, bit for bit the fp64
+            // points of sample_point)
             const bool sys = p.mode == MODE_SYSTEMATIC;
             if (sys) {
                 for (int h = pt; h < G; h += NPT) {
@@ -446,15 +447,14 @@ __global__ void __launch_bounds__(CL_NT, 1)
 #pragma unroll
             for (int h = 0; h < G; ++h) w0[h] = sys ? tfx[h * S] : 0;
             asm volatile("bar.sync %0, %1;" ::"n"(CL_PTS_BAR), "n"(NPT) : "memory");
+            const uint64_t rsb = (uint64_t)__double_as_longlong(p.rS);
             for (int i = pt; i < G * S; i += NPT) {
                 const int h = i / S, si = i % S;
                 uint64_t wh = 0;
 #pragma unroll
                 for (int k = 0; k < G; ++k)
                     if (k == h) wh = w0[k];
-                const double t = sys ? __dmul_rn(__dadd_rn(word_uniform(wh), (double)si), p.rS)
-                                     : __dmul_rn(__dadd_rn((double)si, word_uniform(tfx[i])), p.rS);
-                tfx[i] = __double2ull_rz(__dmul_rn(t, 0x1p64));
+                tfx[i] = point_fraction(si, sys ? wh : tfx[i], rsb);
             }
         }
     }

@@ -272,6 +272,43 @@ __device__ __forceinline__ double word_uniform(uint64_t x)
     return __dmul_rn(__uint2double_rn((uint32_t)(x >> 32)), 0x1p-32);
 }
 
+// floor(t 2^64) of the sample point t = (s + u) rS, u = (word >> 32) 2^-32 the word's
+// 32-bit uniform and rS = rs_bits as a positive normal double, bit for bit as IEEE double
+// arithmetic evaluates it (u + s, then one multiply rounded to nearest even, then the
+// exact scaling by 2^64 truncated) -- but in integers, with no fp64 unit.  For 0 <= s <
+// 2^20: (s + u) 2^32 is an exact integer y of at most 52 bits, rS = M 2^(E - 1075) with a
+// 53-bit M, and their product P = y M (at most 105 bits) is rounded to 53 bits.
+__host__ __device__ inline uint64_t point_fraction(int s, uint64_t word, uint64_t rs_bits)
+{
+    const uint64_t y = ((uint64_t)(uint32_t)s << 32) | (word >> 32);
+    if (y == 0) return 0;
+    const uint64_t M = (rs_bits & ((1ull << 52) - 1)) | (1ull << 52);
+    const int E = (int)((rs_bits >> 52) & 0x7ff);
+#ifdef __CUDA_ARCH__
+    const uint64_t hi = __umul64hi(y, M), lo = y * M;
+    const int nb = hi ? 128 - __clzll((long long)hi) : 64 - __clzll((long long)lo);
+#else
+    const unsigned __int128 P = (unsigned __int128)y * M;
+    const uint64_t hi = (uint64_t)(P >> 64), lo = (uint64_t)P;
+    const int nb = hi ? 128 - __builtin_clzll(hi) : 64 - __builtin_clzll(lo);
+#endif
+    int r = nb > 53 ? nb - 53 : 0;  // bits rounded off (at most 52)
+    uint64_t q = lo;
+    if (r > 0) {
+        q = (lo >> r) | (hi << (64 - r));
+        const uint64_t half = (lo >> (r - 1)) & 1u;                         // the first bit off
+        const bool sticky = (lo & ((1ull << (r - 1)) - 1u)) != 0;           // any bit below it
+        if (half && (sticky || (q & 1u))) ++q;
+        if (q >> 53) {  // rounded up to 2^53
+            q >>= 1;
+            ++r;
+        }
+    }
+    // t = q 2^(r - 32 + E - 1075), so t 2^64 = q 2^(r + E - 1043) (below 2^64: t < 1)
+    const int sh = r + E - 1043;
+    return sh >= 0 ? (q << sh) : (sh <= -64 ? 0 : (q >> -sh));
+}
+
 // Philox block (blk, b, h, domain) keyed by (seed, 0).
 __device__ __forceinline__ void philox_block(uint64_t seed, uint64_t blk, int b, int h, uint64_t dom,
                                              uint64_t out[4])

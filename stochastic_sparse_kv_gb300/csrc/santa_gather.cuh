@@ -212,8 +212,8 @@ __device__ __forceinline__ void value_prologue(const Params &p, int bh, uint8_t 
     } else {
         // The Philox blocks, each drawn once: one per head (systematic: every point shares
         // its uniform), or one per four points (stratified: the raw words wait in the point
-        // array until each thread replaces its own with its point).  Then the fp64 point
-        // as a 64-bit fraction (t < 1; the scaling by 2^64 is exact), as sample_point.
+        // array until each thread replaces its own with its point).  Then each point as a
+        // 64-bit fraction, bit for bit the fp64 point of sample_point, in integers.
         const bool sys = p.mode == MODE_SYSTEMATIC;
         uint64_t *w0 = reinterpret_cast<uint64_t *>(misc + GM_SCAN);
         if (sys) {
@@ -232,11 +232,8 @@ __device__ __forceinline__ void value_prologue(const Params &p, int bh, uint8_t 
             }
         }
         team_sync<BAR, NTH>();
-        for (int s = tid; s < S; s += NTH) {
-            const double t = sys ? __dmul_rn(__dadd_rn(word_uniform(*w0), (double)s), p.rS)
-                                 : __dmul_rn(__dadd_rn((double)s, word_uniform(tfx[s])), p.rS);
-            tfx[s] = __double2ull_rz(__dmul_rn(t, 0x1p64));
-        }
+        const uint64_t rsb = (uint64_t)__double_as_longlong(p.rS);
+        for (int s = tid; s < S; s += NTH) tfx[s] = point_fraction(s, sys ? *w0 : tfx[s], rsb);
     }
     for (int i = tid; i < D; i += NTH) qf[i] = __uint_as_float((uint32_t)p.q[(size_t)bh * D + i] << 16);
     if (tid == 0) {
