@@ -87,3 +87,19 @@ def test_stamped_run_on_the_gpu(two_pass):
         assert r["value_ctas"] == 32 and r["value_wait_done"]["min"] >= m["cta end"]["min"]
     else:
         assert r["ctas"] >= 8
+
+
+def test_stamped_build_compiles_and_takes_a_buffer():
+    # the stamped library (not part of build()) must keep compiling; its setter only
+    # records the pointer, so it runs without a GPU
+    import shutil
+    if not (shutil.which("nvcc") or os.path.exists("/usr/local/cuda/bin/nvcc")):
+        pytest.skip("nvcc not found")
+    from stochastic_sparse_kv_gb300 import _build
+    lib = ctypes.CDLL(_build.build(timeline=True))
+    lib.santa_timeline_buffer.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    buf = ctypes.create_string_buffer(16 * 8 * (timeline.ROWS_SCORE + 64))
+    assert lib.santa_timeline_buffer(ctypes.addressof(buf), len(buf)) == 0
+    assert lib.santa_timeline_buffer(ctypes.addressof(buf), 16) == -1        # too small
+    assert lib.santa_timeline_buffer(ctypes.addressof(buf) + 4, len(buf) - 8) == -2  # misaligned
+    assert lib.santa_timeline_buffer(None, 0) == 0
