@@ -7,6 +7,14 @@ JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+The line carries the headline (`value`, µs per step, one pair of CUDA events around the
+timed steps), `roofline` (algorithmic bytes per call over the measured copy peak, and the
+DRAM traffic of an ncu record taken on the same sources), `clocks` sampled during the
+timed region, `e2e` (host buffers copied in and out every step), `cpu_baseline` (the
+oracle) and `gpu_launches`.  Unless --no-extras: the other sampling modes and dense, S
+sweeps, Bernoulli qK^T, group dedup, a 32-layer CUDA-graph stack and (unless
+--no-workloads) every other configuration of the workload table.
+
 --impl reference times the fp64 CPU oracle on this machine's host cores on a bounded
 sample of the same workload, scaled to the same unit.
 """
